@@ -1,0 +1,418 @@
+"""Benchmark of the ternary FFN decode step on GB300.
+
+One "step" is one full FFN layer decode step (rotate+quantise x -> gate/up
+ternary GEMVs + SiLU*up -> rotate+quantise h -> down GEMV) at hidden 5120,
+intermediate 17408, batch 1, 2-bit ternary weights: the dense-FFN shape of a
+27B ternary model.  Inputs are seeded synthetic data (see
+ternary_weight_dp4a_gb300/synth.py).  The headline value is weight bytes
+streamed per second (GB/s) with inputs resident in HBM; eight independently
+seeded weight sets (568 MB, more than 4x the 129 MB L2) are used in rotation so
+every step streams its weights from HBM.
+
+Prints ONE JSON line on rank 0.  Launch with torchrun for N > 1 GPUs: each rank
+runs an independent replica (the decode FFN needs no exchange between GPUs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HIDDEN, INTER = 5120, 17408
+N_SETS = 8
+METRIC = "ternary FFN decode step: weight GB/s & % HBM roofline, µs/token at batch 1/2/4/8"
+WORKLOAD = "ffn_layer_h5120_i17408_ternary2"
+BLOCK = 128
+
+
+def layer_bytes(hidden: int, inter: int, fmt: int) -> int:
+    """Algorithmic bytes of one FFN layer: packed codes + fp16 scales of gate, up, down."""
+    per = 4 if fmt == 0 else 8
+    one = inter * hidden // per + 2 * inter * (hidden // BLOCK)
+    return 3 * one
+
+
+def gateup_bytes(hidden: int, inter: int, fmt: int) -> int:
+    per = 4 if fmt == 0 else 8
+    return 2 * (inter * hidden // per + 2 * inter * (hidden // BLOCK))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ternary_weight_dp4a_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, or None
+    if there is none or the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        loaded = [r for r in rows if num(r[3]) is not None and num(r[3]) > 300.0] or rows
+        sm_loaded = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm_loaded or sm) if (sm_loaded or sm) else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": reasons, "samples": len(rows),
+                "samples_under_load": len(loaded),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_weights(fmt: int, sets: int, hidden: int, inter: int, seed_layer0: int = 0):
+    """``sets`` independently seeded FFN layers, packed on the device."""
+    import torch
+    from ternary_weight_dp4a_gb300 import synth, tq
+    layers = []
+    for l in range(sets):
+        mats = []
+        for j, (n, k) in enumerate([(inter, hidden), (inter, hidden), (hidden, inter)]):
+            codes, scales = synth.weight(n, k, fmt, synth.ffn_weight_seed(seed_layer0 + l, j),
+                                         device="cuda")
+            mats.append(tq.pack_weights(codes, fmt, scales))
+            del codes
+        layers.append(mats)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layers
+
+
+def time_graph(fn_steps, reps: int, warmup_reps: int, world: int, sampler_gpu=None):
+    """Capture fn_steps() (one pass over the weight sets) in a CUDA graph, replay
+    it ``reps`` times in the timed region; returns (ms total, clock summary)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn_steps()                      # eager warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn_steps()
+    for _ in range(warmup_reps):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = None
+    ctx = ClockSampler(sampler_gpu) if sampler_gpu is not None else None
+    if ctx:
+        ctx.__enter__()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(reps):
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    if ctx:
+        ctx.__exit__(None, None, None)
+        clocks = ctx.summary()
+    return start.elapsed_time(end), clocks
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    from ternary_weight_dp4a_gb300 import build as tqbuild
+    from ternary_weight_dp4a_gb300 import synth, tq
+
+    tqbuild.build()
+    tq.load()
+    fmt = tq.FMT_TERNARY2
+    peak, peak_kind = load_peaks()
+    lb = layer_bytes(HIDDEN, INTER, fmt)
+    layers = make_weights(fmt, N_SETS, HIDDEN, INTER)
+    xs = {m: synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
+          for m in (1, 2, 4, 8)}
+    ys = {m: torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda") for m in xs}
+    wss = {m: tq.ffn_workspace(m, HIDDEN, INTER) for m in xs}
+
+    def one_pass(m):
+        def f():
+            for g, u, d in layers:
+                tq.ffn_step(g, u, d, xs[m], y=ys[m], workspace=wss[m])
+        return f
+
+    # --- headline: m = 1, K steps (graph of one pass over the N_SETS layers) ---
+    reps = max(1, args.steps // N_SETS)
+    steps = reps * N_SETS
+    warm_reps = max(1, -(-args.warmup // N_SETS))
+    ms, clocks = time_graph(one_pass(1), reps, warm_reps, world, sampler_gpu=local)
+    ms = max_over_ranks(ms, world)
+    ms_step = ms / steps
+    value = world * lb / (ms_step * 1e-3) / 1e9
+
+    # --- batch sweep m = 1, 2, 4, 8 (same weights, packed rows) ---
+    sweep = {}
+    sweep_reps = max(1, min(reps, 2000 // N_SETS))
+    for m in (1, 2, 4, 8):
+        t, _ = time_graph(one_pass(m), sweep_reps, 2, world)
+        t = max_over_ranks(t, world)
+        us = t * 1e3 / (sweep_reps * N_SETS)
+        sweep[f"m{m}"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
+                          "tokens_per_s": round(m * 1e6 / us, 1),
+                          "hbm_frac": round(lb / us / 1e3 / peak, 4)}
+
+    # --- roofline: the dominant kernel (fused gate/up GEMV), event-timed ---
+    gu_bytes = gateup_bytes(HIDDEN, INTER, fmt)
+    q1, s1 = tq.rotate_quant(xs[1])
+    h1 = torch.empty((1, INTER), dtype=torch.bfloat16, device="cuda")
+    n_gu = max(N_SETS, min(steps, 4000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_gu)]
+    for i in range(2 * N_SETS):
+        g, u, _ = layers[i % N_SETS]
+        tq.ffn_gateup(g, u, q1, s1, h=h1)
+    torch.cuda.synchronize()
+    for i, (e0, e1) in enumerate(evs):
+        g, u, _ = layers[i % N_SETS]
+        e0.record()
+        tq.ffn_gateup(g, u, q1, s1, h=h1)
+        e1.record()
+    torch.cuda.synchronize()
+    gu_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    gu_achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+
+    # --- end to end through the public API with host buffers ---
+    x_host = xs[1].cpu().pin_memory()
+    y_host = torch.empty((1, HIDDEN), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(xs[1])
+    e2e_steps = max(N_SETS, min(steps, 2000))
+    for i in range(N_SETS):
+        g, u, d = layers[i % N_SETS]
+        x_dev.copy_(x_host, non_blocking=True)
+        tq.ffn_step(g, u, d, x_dev, y=ys[1], workspace=wss[1])
+        y_host.copy_(ys[1], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        g, u, d = layers[i % N_SETS]
+        x_dev.copy_(x_host, non_blocking=True)
+        tq.ffn_step(g, u, d, x_dev, y=ys[1], workspace=wss[1])
+        y_host.copy_(ys[1], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    barrier(world)
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall_ms), world) / e2e_steps
+    e2e_value = world * lb / (e2e_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm_reps * N_SETS,
+        "ms_per_step": round(ms_step, 6),
+        "us_per_token_m1": round(ms_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8xternary2->f32",
+        "data": "synthetic (seeded; ternary p0=0.4, fp16 scales U[0.01,0.05], bf16 N(0,1) x, 1% x10 outliers)",
+        "config": {"workload": WORKLOAD, "hidden": HIDDEN, "intermediate": INTER, "m": 1,
+                   "weight_format": "2-bit ternary, 128-blocks, fp16 scales",
+                   "bytes_per_step": lb, "weight_sets": N_SETS,
+                   "l2": f"{N_SETS} weight sets rotated ({N_SETS * lb / 1e6:.0f} MB > 129 MB L2)",
+                   "timing": "CUDA graph of one pass over the weight sets, replayed; CUDA events",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_frac": round(value / world / peak, 4),
+        "sweep": sweep,
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<0,1,2> (fused gate/up + SiLU*up)",
+                     "achieved": round(gu_achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gu_achieved / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_ms * 1e3, 3),
+                     "traffic": recorded_traffic("gateup_m1")},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                "us_per_step": round(e2e_ms * 1e3, 3),
+                "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4},
+        "gpu_launches": steps * 4,
+        "clocks": clocks,
+    }
+    return result
+
+
+def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1):
+    """Time the oracle's FFN step on the host cores on a bounded sample: as many
+    full layer steps (m rows) as fit in about ``budget_s`` seconds."""
+    from oracle import oracle
+    from ternary_weight_dp4a_gb300 import synth
+    oracle.build()
+    mats = []
+    for j, (n, k) in enumerate([(INTER, HIDDEN), (INTER, HIDDEN), (HIDDEN, INTER)]):
+        codes, scales = synth.weight(n, k, fmt, synth.ffn_weight_seed(0, j))
+        mats.extend([oracle.pack(codes, fmt), scales])
+        del codes
+    x = synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01)
+    lb = layer_bytes(HIDDEN, INTER, fmt)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.ffn_step(*mats, fmt, HIDDEN, INTER, x)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / steps * (steps + 1) > 2 * budget_s:
+            break
+    return {"value": round(lb * steps / el / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"{steps} full FFN layer step(s), m={m}, hidden {HIDDEN}, "
+                      f"intermediate {INTER}, 2-bit; {el:.1f} s",
+            "us_per_step": round(el / steps * 1e6, 1)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle, timed on rank 0's host cores only
+        if rank != 0:
+            return
+        base = cpu_oracle_baseline(args.cpu_budget)
+        steps = max(1, args.steps if args.steps < 4 else 1)
+        line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
+                "n_gpus": world, "steps": steps, "warmup": 0,
+                "ms_per_step": round(base["us_per_step"] / 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int8xternary2->f32",
+                "data": "synthetic (seeded)",
+                "config": {"workload": WORKLOAD, "hidden": HIDDEN, "intermediate": INTER, "m": 1},
+                "cpu_baseline": base,
+                "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    rank, world, local = dist_setup()
+    result = run_ours(args, rank, world, local)
+    if rank == 0:
+        result["cpu_baseline"] = cpu_oracle_baseline(args.cpu_budget)
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

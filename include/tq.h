@@ -1,0 +1,159 @@
+/*
+ * tq.h -- C ABI of libtq, the GB300 (sm_103a) ternary-weight FFN decode library.
+ *
+ * The operation is the decode-time FFN of a ternary-weight model read "from
+ * its stored ternary blocks ... through a dp4a GEMV with its int8 activation
+ * staged in shared memory and produced by the Hadamard rotation", with
+ * "packed steps of up to 8 rows ... each row bit-identical to its single-row
+ * decode" (sparkinfer PR #1154, "decode and small packed batches read the FFN
+ * from a ternary copy through a dp4a GEMV", Summary).
+ *
+ * Conventions for every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates no memory and keeps no device state between calls.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream).  No call synchronises the stream or the device.
+ *   - Arrays are row-major and contiguous.  A call checks its arguments
+ *     before launching anything; on an error nothing is launched and the
+ *     outputs are untouched.
+ *   - TQ_ERR_CUDA means a launch itself failed; tq_last_cuda_error() gives
+ *     the cudaError_t of the most recent failure on the calling thread.
+ *     Errors raised later by kernels in flight surface at the caller's next
+ *     synchronisation, as for any CUDA call.
+ *   - Outputs must not overlap inputs or each other.
+ *   - Sizes: k and hidden/intermediate are multiples of 128; 1 <= m <= 8.
+ *   - Floating point is IEEE binary32 with the rounding of each step
+ *     documented at the entry point; results do not depend on m, on the
+ *     stream or on how many SMs the GPU has.
+ *
+ * Weight layout (the pages fix none; this library fixes this one):
+ *   TQ_FMT_TERNARY2: 2-bit codes, 4 per byte.  Weight j of row i is in byte
+ *     i*(k/4) + j/4 at bits 2*(j%4)..2*(j%4)+1, least significant first;
+ *     code 0 -> 0, 1 -> +1, 2 -> -1 (3 must not occur; it reads as 0).
+ *   TQ_FMT_BINARY1: 1 bit per weight, 8 per byte.  Weight j of row i is bit
+ *     j%8 of byte i*(k/8) + j/8; 1 -> +1, 0 -> -1.
+ *   scales: one IEEE fp16 per 128-weight block per row, [n][k/128].
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *tq_stream_t;
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1, /* null pointer, size out of range, shape mismatch   */
+    TQ_ERR_ALIGNMENT = 2,   /* a pointer lacks the alignment its argument needs */
+    TQ_ERR_UNSUPPORTED = 3, /* valid but beyond this build's limits              */
+    TQ_ERR_WORKSPACE = 4,   /* workspace smaller than tq_ffn_workspace_bytes()   */
+    TQ_ERR_CUDA = 5         /* a CUDA runtime call or launch failed              */
+} tq_status;
+
+typedef enum { TQ_FMT_TERNARY2 = 0, TQ_FMT_BINARY1 = 1 } tq_format;
+
+/* One packed weight matrix W [n][k] in the layout above.
+ * codes: 32-byte aligned.  scales: 2-byte aligned. */
+typedef struct {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    int32_t n;
+    int32_t k;
+    int32_t fmt; /* tq_format */
+} tq_weight;
+
+/* Most activation rows in one packed step.  The GEMV also needs
+ * m * (k/128) * 152 bytes (156 for 1-bit) of shared memory per CTA, at most
+ * the device's opt-in limit (227 KB on GB300: k <= 24448 at m = 8);
+ * beyond it a call returns TQ_ERR_UNSUPPORTED. */
+#define TQ_MAX_ROWS 8
+
+/* Human-readable name of a status code (static string). */
+const char *tq_status_string(tq_status s);
+
+/* cudaError_t of the last failed CUDA call made by this library on the
+ * calling thread (0 if none). */
+int tq_last_cuda_error(void);
+
+/* Pack weight codes into the layout above (a load-time step).
+ * codes: uint8 [n][k]; for TQ_FMT_TERNARY2 each entry is 0, 1 or 2 (value
+ * 0, +1, -1), for TQ_FMT_BINARY1 each entry is 0 or 1 (value -1, +1).  Only
+ * the low 2 (resp. 1) bits of each entry are read.
+ * packed: [n][k/4] or [n][k/8] bytes, 32-byte aligned. */
+tq_status tq_pack_weights(const uint8_t *codes, int32_t n, int32_t k, int32_t fmt,
+                          uint8_t *packed, tq_stream_t stream);
+
+/* Rotate and quantise activations ("the Hadamard rotation emits that int8
+ * copy", PR #1154 Summary).  For each row r and 128-block b of x (bf16 bits
+ * [m][k]): v = H128 * x_block in fp32, computed as the fast transform's
+ * butterflies for span 1, 2, 4, ..., 64 (a+b to the lower index, a-b to the
+ * upper) followed by one multiply by (float)(1/sqrt(128)); then
+ * s[r][b] = max|v| / 127 and q = round-half-even(v / s) clamped to
+ * [-127, 127] (IEEE division); an all-zero block gives s = 0, q = 0.
+ * q: int8 [m][k], 16-byte aligned.  s: fp32 [m][k/128].  x: 16-byte aligned.
+ * 1 <= m <= 8 is not required here: any m >= 1. */
+tq_status tq_rotate_quant(const uint16_t *x, int32_t m, int32_t k, int8_t *q, float *s,
+                          tq_stream_t stream);
+
+/* Ternary/binary GEMV for a packed step of m rows (the "dp4a GEMV", PR #1154
+ * Summary).  For row r and output i:
+ *   d_b = sum_{j in block b} W[i][j] * q[r][j]          (exact int32)
+ *   t_b = (float)d_b * (fp16->fp32(scales[i][b]) * s[r][b])
+ *   y[r][i] = ((P0+P1)+(P2+P3)) + ((P4+P5)+(P6+P7)),
+ *   P_p = (((0 + t_p) + t_{p+8}) + t_{p+16}) + ...      (fp32, ascending b)
+ * which is the same for every m, so each row of a packed step is
+ * bit-identical to its single-row result.
+ * q: int8 [m][k] (16-byte aligned); s: fp32 [m][k/128]; y: fp32 [m][n].
+ * blockdots: NULL, or int32 [m][n][k/128] receiving every d_b. */
+tq_status tq_gemv(const tq_weight *w, const int8_t *q, const float *s, int32_t m, float *y,
+                  int32_t *blockdots, tq_stream_t stream);
+
+/* The fused gate/up stage of the FFN step: for each row r and output i,
+ *   g = gemv(gate, qx, sx)[r][i], u = gemv(up, qx, sx)[r][i]  (as tq_gemv)
+ *   h[r][i] = bf16_rn(g / (1 + exp(-g)) * u)                   (as tq_ffn_step)
+ * gate, up: [inter][hidden], same format; qx int8 [m][hidden] (16-byte
+ * aligned); sx fp32 [m][hidden/128]; h: bf16 bits [m][inter]. */
+tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t *qx,
+                        const float *sx, int32_t m, uint16_t *h, tq_stream_t stream);
+
+/* Bytes of device workspace tq_ffn_step needs for these sizes. */
+size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter);
+
+/* One decode FFN step for m packed rows:
+ *   (qx, sx) = rotate_quant(x)                           [m][hidden]
+ *   g = gemv(gate, qx, sx), u = gemv(up, qx, sx)         [m][inter]
+ *   h = bf16_rn(g / (1 + exp(-g)) * u)                   [m][inter]
+ *   (qh, sh) = rotate_quant(h);  y = gemv(down, qh, sh)  [m][hidden]
+ * gate, up: [inter][hidden]; down: [hidden][inter]; all the same format.
+ * exp(z) is computed as 2^n * P(r): n = round-half-even(z * log2 e),
+ * r = fma(-n, L2, fma(-n, L1, z)) with L1 = ln 2 with its low 12 significand
+ * bits cleared and L2 = ln 2 - L1, P the degree-7 Taylor polynomial by
+ * Horner's rule with fused multiply-adds; z > 88.72283935546875 gives +inf,
+ * z < -103.972084045410156 gives 0.  Division is IEEE.
+ * x: bf16 bits [m][hidden], 16-byte aligned.  y: fp32 [m][hidden].
+ * workspace: >= tq_ffn_workspace_bytes(m, hidden, inter) bytes, 256-byte
+ * aligned; its contents on entry do not matter and are garbage on exit. */
+tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
+                      const uint16_t *x, int32_t m, float *y, void *workspace,
+                      size_t workspace_bytes, tq_stream_t stream);
+
+/* RMS-normalise (between stacked layers): for each row r,
+ *   ss = sum_i y[r][i]^2 as 256 partial sums (partial t adds i = t, t+256, ...
+ *        in ascending order from +0.0) combined pairwise at distance
+ *        1, 2, 4, ..., 128;
+ *   x_out[r][i] = bf16_rn(y[r][i] * (1 / sqrt(ss / n + eps)))
+ * with IEEE sqrt and division.  y: fp32 [m][n]; x_out: bf16 bits [m][n]. */
+tq_status tq_rmsnorm_bf16(const float *y, int32_t m, int32_t n, float eps, uint16_t *x_out,
+                          tq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

@@ -1,0 +1,198 @@
+"""ctypes binding of libtq (include/tq.h).  Argument marshalling only.
+
+Every function takes torch CUDA tensors (PyTorch provides device memory and
+streams), passes raw device pointers to the C ABI and raises ``TQError`` on a
+non-OK status.  Work is enqueued on the current torch CUDA stream unless a
+``stream`` is given.  There is no CPU path: if ``libtq.so`` has not been built
+(``python -m ternary_weight_dp4a_gb300.build``), the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtq.so")
+
+FMT_TERNARY2 = 0
+FMT_BINARY1 = 1
+BLOCK = 128
+MAX_ROWS = 8
+
+# every entry point include/tq.h declares
+EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",
+           "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_step",
+           "tq_rmsnorm_bf16")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TQError(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        name = load().tq_status_string(status).decode()
+        extra = f" (cudaError {cuda_error})" if status == 5 else ""
+        super().__init__(f"{fn}: {name}{extra}")
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("n", ctypes.c_int32), ("k", ctypes.c_int32), ("fmt", ctypes.c_int32)]
+
+
+def load():
+    """Load libtq.so (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libtq.so not found at {LIB_PATH}: build it with "
+                    "`python -m ternary_weight_dp4a_gb300.build` (needs nvcc); "
+                    "there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+            W = ctypes.POINTER(_Weight)
+            L.tq_status_string.argtypes = [ctypes.c_int]
+            L.tq_status_string.restype = ctypes.c_char_p
+            L.tq_last_cuda_error.restype = ctypes.c_int
+            L.tq_pack_weights.argtypes = [vp, i32, i32, i32, vp, vp]
+            L.tq_rotate_quant.argtypes = [vp, i32, i32, vp, vp, vp]
+            L.tq_gemv.argtypes = [W, vp, vp, i32, vp, vp, vp]
+            L.tq_ffn_gateup.argtypes = [W, W, vp, vp, i32, vp, vp]
+            L.tq_ffn_workspace_bytes.argtypes = [i32, i32, i32]
+            L.tq_ffn_workspace_bytes.restype = sz
+            L.tq_ffn_step.argtypes = [W, W, W, vp, i32, vp, vp, sz, vp]
+            L.tq_rmsnorm_bf16.argtypes = [vp, i32, i32, f32, vp, vp]
+            for name in EXPORTS:
+                if name != "tq_status_string" and name != "tq_last_cuda_error" and \
+                        name != "tq_ffn_workspace_bytes":
+                    getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise TQError(fn, status, load().tq_last_cuda_error())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+@dataclass
+class PackedWeight:
+    """A packed weight matrix on the device: codes [n][k/4] (2-bit) or
+    [n][k/8] (1-bit) uint8, scales [n][k/128] float16."""
+    codes: "object"
+    scales: "object"
+    n: int
+    k: int
+    fmt: int
+
+    def c_struct(self) -> _Weight:
+        return _Weight(self.codes.data_ptr(), self.scales.data_ptr(), self.n, self.k, self.fmt)
+
+    @property
+    def nbytes(self) -> int:
+        return self.codes.numel() + 2 * self.scales.numel()
+
+
+def pack_weights(codes, fmt: int, scales, stream=None) -> PackedWeight:
+    """codes: uint8 CUDA tensor [n][k]; scales: float16 CUDA tensor [n][k/128]."""
+    import torch
+    n, k = codes.shape
+    per = 4 if fmt == FMT_TERNARY2 else 8
+    packed = torch.empty((n, k // per), dtype=torch.uint8, device=codes.device)
+    _check("tq_pack_weights", load().tq_pack_weights(_ptr(codes), n, k, fmt, _ptr(packed),
+                                                      _stream(stream)))
+    return PackedWeight(packed, scales.contiguous(), n, k, fmt)
+
+
+def rotate_quant(x, q=None, s=None, stream=None):
+    """x: bf16 CUDA tensor [m][k] -> (q int8 [m][k], s float32 [m][k/128])."""
+    import torch
+    m, k = x.shape
+    if q is None:
+        q = torch.empty((m, k), dtype=torch.int8, device=x.device)
+    if s is None:
+        s = torch.empty((m, k // BLOCK), dtype=torch.float32, device=x.device)
+    _check("tq_rotate_quant", load().tq_rotate_quant(_ptr(x), m, k, _ptr(q), _ptr(s),
+                                                      _stream(stream)))
+    return q, s
+
+
+def gemv(w: PackedWeight, q, s, y=None, blockdots: bool = False, stream=None):
+    """y[m][n] (float32); with ``blockdots`` also the int32 [m][n][k/128] dots."""
+    import torch
+    m = q.shape[0]
+    if y is None:
+        y = torch.empty((m, w.n), dtype=torch.float32, device=q.device)
+    d = torch.empty((m, w.n, w.k // BLOCK), dtype=torch.int32, device=q.device) \
+        if blockdots else None
+    ws = w.c_struct()
+    _check("tq_gemv", load().tq_gemv(ctypes.byref(ws), _ptr(q), _ptr(s), m, _ptr(y), _ptr(d),
+                                     _stream(stream)))
+    return (y, d) if blockdots else y
+
+
+def ffn_gateup(gate: PackedWeight, up: PackedWeight, qx, sx, h=None, stream=None):
+    """Fused gate/up GEMVs + SiLU(g)*u: qx int8 [m][hidden] -> h bf16 [m][inter]."""
+    import torch
+    m = qx.shape[0]
+    if h is None:
+        h = torch.empty((m, gate.n), dtype=torch.bfloat16, device=qx.device)
+    g, u = gate.c_struct(), up.c_struct()
+    _check("tq_ffn_gateup", load().tq_ffn_gateup(ctypes.byref(g), ctypes.byref(u), _ptr(qx),
+                                                 _ptr(sx), m, _ptr(h), _stream(stream)))
+    return h
+
+
+def ffn_workspace_bytes(m: int, hidden: int, inter: int) -> int:
+    return int(load().tq_ffn_workspace_bytes(m, hidden, inter))
+
+
+def ffn_workspace(m: int, hidden: int, inter: int, device="cuda"):
+    import torch
+    return torch.empty(ffn_workspace_bytes(m, hidden, inter), dtype=torch.uint8, device=device)
+
+
+def ffn_step(gate: PackedWeight, up: PackedWeight, down: PackedWeight, x, y=None,
+             workspace=None, stream=None):
+    """x: bf16 CUDA tensor [m][hidden] -> y float32 [m][hidden]."""
+    import torch
+    m, hidden = x.shape
+    if y is None:
+        y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = ffn_workspace(m, hidden, gate.n, x.device)
+    g, u, d = gate.c_struct(), up.c_struct(), down.c_struct()
+    _check("tq_ffn_step", load().tq_ffn_step(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d),
+                                             _ptr(x), m, _ptr(y), _ptr(workspace),
+                                             workspace.numel(), _stream(stream)))
+    return y
+
+
+def rmsnorm_bf16(y, eps: float = 1e-6, x_out=None, stream=None):
+    """y float32 [m][n] -> bf16 [m][n]."""
+    import torch
+    m, n = y.shape
+    if x_out is None:
+        x_out = torch.empty((m, n), dtype=torch.bfloat16, device=y.device)
+    _check("tq_rmsnorm_bf16", load().tq_rmsnorm_bf16(_ptr(y), m, n, eps, _ptr(x_out),
+                                                     _stream(stream)))
+    return x_out

@@ -1,0 +1,96 @@
+"""The C-ABI library loads and exports every entry point include/tq.h declares,
+and rejects bad arguments before touching the GPU.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from ternary_weight_dp4a_gb300 import build as tqbuild
+from ternary_weight_dp4a_gb300 import tq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tqbuild.build()
+    return tq.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(tq.EXPORTS) == _declared()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.tq_status_string(0) == b"ok"
+    assert lib.tq_status_string(4) == b"workspace too small"
+    assert lib.tq_status_string(99) == b"unknown status"
+
+
+def test_workspace_bytes(lib):
+    # qx 5120 | sx 160->256 | h 34816 | qh 17408 | sh 544->768, each 256-aligned
+    assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == 5120 + 256 + 34816 + 17408 + 768
+    assert lib.tq_ffn_workspace_bytes(0, 5120, 17408) == 0
+
+
+def _w(codes=0x1000, scales=0x2000, n=512, k=256, fmt=0):
+    return tq._Weight(codes, scales, n, k, fmt)
+
+
+def test_gemv_rejects_bad_arguments_before_any_launch(lib):
+    good_q, good_s, good_y = ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), ctypes.c_void_p(0x5000)
+    st = ctypes.c_void_p(0)
+    call = lambda w, q=good_q, s=good_s, m=1, y=good_y: lib.tq_gemv(ctypes.byref(w), q, s, m, y, None, st)
+    assert call(_w(codes=0)) == 1                       # null codes
+    assert call(_w(k=200)) == 1                         # k not a multiple of 128
+    assert call(_w(n=0)) == 1                           # empty output
+    assert call(_w(fmt=7)) == 1                         # unknown format
+    assert call(_w(), m=0) == 1 and call(_w(), m=9) == 1
+    assert call(_w(), q=ctypes.c_void_p(0)) == 1
+    assert call(_w(codes=0x1010)) == 2                  # codes not 32-byte aligned
+    assert call(_w(), q=ctypes.c_void_p(0x3008)) == 2   # q not 16-byte aligned
+    assert lib.tq_gemv(None, good_q, good_s, 1, good_y, None, st) == 1
+
+
+def test_ffn_step_rejects_bad_arguments(lib):
+    st = ctypes.c_void_p(0)
+    g, u, d = _w(n=512, k=256), _w(n=512, k=256), _w(n=256, k=512)
+    x, y, ws = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    need = lib.tq_ffn_workspace_bytes(1, 256, 512)
+    call = lambda g=g, u=u, d=d, m=1, wsb=need, ws=ws: lib.tq_ffn_step(
+        ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), x, m, y, ws, wsb, st)
+    assert call(d=_w(n=256, k=384)) == 1                # down shape mismatch
+    assert call(u=_w(n=512, k=256, fmt=1)) == 1         # mixed formats
+    assert call(m=9) == 1
+    assert call(wsb=need - 1) == 4                      # workspace too small
+    assert call(ws=ctypes.c_void_p(0x30010)) == 2       # workspace not 256-byte aligned
+
+
+def test_other_entry_points_reject_bad_arguments(lib):
+    st = ctypes.c_void_p(0)
+    p = ctypes.c_void_p(0x1000)
+    assert lib.tq_pack_weights(None, 4, 128, 0, p, st) == 1
+    assert lib.tq_pack_weights(p, 4, 100, 0, p, st) == 1
+    assert lib.tq_pack_weights(p, 4, 128, 0, ctypes.c_void_p(0x1001), st) == 2
+    assert lib.tq_rotate_quant(p, 0, 128, p, p, st) == 1
+    assert lib.tq_rotate_quant(p, 1, 130, p, p, st) == 1
+    assert lib.tq_rmsnorm_bf16(None, 1, 128, ctypes.c_float(1e-6), p, st) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(tq, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(tq, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        tq.load()

@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (per the method's exactness): int8 codes, fp32 activation scales and int32
+block dots bit-exact; fp32 outputs bit-exact against the oracle's documented
+fold order and within max relative error 1e-4 of the fp64 definition; every
+row of a packed step bit-identical to its single-row run; repeated runs
+bit-identical.
+"""
+import numpy as np
+import pytest
+
+from _util import Mat, bf16_bits, bf16_tensor, ffn_mats, rel_err, ws_offsets
+from ternary_weight_dp4a_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ternary_weight_dp4a_gb300 import build, tq as tqmod
+    build.build()
+    tqmod.load()
+    return tqmod
+
+
+def _acts(m, k, outliers=0.01, seed=synth.SEED_ACT_BASE):
+    return synth.activation(m, k, seed=seed, outlier_frac=outliers)
+
+
+# ----------------------------------------------------------------------------
+# packing and rotation
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("n,k", [(512, 256), (77, 1152), (300, 5120)])
+def test_pack_bit_exact(tq, orc, fmt, n, k):
+    w = Mat(n, k, fmt, seed=5)
+    assert np.array_equal(w.dev.codes.cpu().numpy(), w.orc_packed(orc))
+
+
+@pytest.mark.parametrize("m,k,outliers", [(1, 256, 0.0), (8, 5120, 0.01), (3, 17408, 0.01),
+                                          (5, 128, 0.0), (13, 384, 0.01)])
+def test_rotate_quant_bit_exact(tq, orc, m, k, outliers):
+    x = _acts(m, k, outliers)
+    if m >= 3:
+        x[1, :128] = 0                      # an all-zero block
+        x[2, 128:256] = 0x4f00 if k >= 256 else x[2, 128:256]   # large bf16 values (2^31)
+    q, s = tq.rotate_quant(bf16_tensor(x))
+    q_ref, s_ref = orc.rotate_quant(x)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------
+# GEMV
+# ----------------------------------------------------------------------------
+
+GEMV_SHAPES = [(512, 256), (1000, 384), (77, 1152), (4101, 5120), (96, 17408)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("n,k", GEMV_SHAPES)
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_gemv_bit_exact(tq, orc, fmt, n, k, m):
+    import torch
+    w = Mat(n, k, fmt, seed=synth.SEED_TINY_WEIGHT)
+    x = _acts(m, k, 0.01)
+    q_ref, s_ref = orc.rotate_quant(x)
+    q = torch.from_numpy(q_ref).cuda()
+    s = torch.from_numpy(s_ref).cuda()
+    y, dots = tq.gemv(w.dev, q, s, blockdots=True)
+    torch.cuda.synchronize()
+    packed = w.orc_packed(orc)
+    d_ref = orc.blockdots(packed, fmt, n, k, q_ref)
+    assert np.array_equal(dots.cpu().numpy(), d_ref)
+    y_ref = orc.gemv(packed, w.scales, fmt, n, k, q_ref, s_ref)
+    yg = y.cpu().numpy()
+    assert np.array_equal(yg.view(np.uint32), y_ref.view(np.uint32))
+    assert rel_err(yg, orc.gemv_f64(packed, w.scales, fmt, n, k, q_ref, s_ref)) <= TOL
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gemv_tiny_config_edge_cases(tq, orc, fmt):
+    """K=256, N=512 (the tiny GEMV), plus zero activations and zero weights."""
+    import torch
+    n, k = 512, 256
+    w = Mat(n, k, fmt, seed=synth.SEED_TINY_WEIGHT)
+    q = torch.zeros((2, k), dtype=torch.int8, device="cuda")
+    s = torch.zeros((2, k // 128), dtype=torch.float32, device="cuda")
+    assert torch.all(tq.gemv(w.dev, q, s) == 0)
+    if fmt == 0:
+        zero_codes = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
+        scales = torch.from_numpy(w.scales).cuda()
+        wz = tq.pack_weights(zero_codes, 0, scales)
+        x = _acts(1, k, 0.0)
+        qq, ss = tq.rotate_quant(bf16_tensor(x))
+        assert torch.all(tq.gemv(wz, qq, ss) == 0)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gemv_packed_rows_bit_identical_to_single(tq, fmt):
+    import torch
+    n, k = 2053, 5120
+    w = Mat(n, k, fmt, seed=17)
+    x = bf16_tensor(_acts(8, k, 0.01))
+    q, s = tq.rotate_quant(x)
+    singles = [tq.gemv(w.dev, q[r:r + 1].contiguous(), s[r:r + 1].contiguous()) for r in range(8)]
+    for m in (2, 3, 4, 5, 6, 7, 8):
+        y = tq.gemv(w.dev, q[:m].contiguous(), s[:m].contiguous())
+        for r in range(m):
+            assert torch.equal(y[r].view(torch.int32), singles[r][0].view(torch.int32)), (m, r)
+
+
+# ----------------------------------------------------------------------------
+# FFN step
+# ----------------------------------------------------------------------------
+
+def _ffn_gpu(tq, mats, x_bits):
+    import torch
+    g, u, d = mats
+    m, hidden = x_bits.shape
+    ws = tq.ffn_workspace(m, hidden, g.n)
+    y = tq.ffn_step(g.dev, u.dev, d.dev, bf16_tensor(x_bits), workspace=ws)
+    torch.cuda.synchronize()
+    return y.cpu().numpy(), ws
+
+
+def _ffn_orc(orc, mats, x_bits):
+    g, u, d = mats
+    return orc.ffn_step(g.orc_packed(orc), g.scales, u.orc_packed(orc), u.scales,
+                        d.orc_packed(orc), d.scales, g.fmt, d.n, g.n, x_bits)
+
+
+def _check_ffn(tq, orc, mats, x_bits):
+    m, hidden = x_bits.shape
+    inter = mats[0].n
+    y, ws = _ffn_gpu(tq, mats, x_bits)
+    ref = _ffn_orc(orc, mats, x_bits)
+    # stage-wise first (diagnoses which stage differs), then the output
+    o = ws_offsets(m, hidden, inter)
+    wsn = ws.cpu().numpy()
+    assert np.array_equal(wsn[o["qx"]:o["qx"] + m * hidden].view(np.int8).reshape(m, hidden),
+                          ref["qx"])
+    h = wsn[o["h"]:o["h"] + 2 * m * inter].view(np.uint16).reshape(m, inter)
+    assert np.array_equal(h, ref["h"])
+    assert np.array_equal(wsn[o["qh"]:o["qh"] + m * inter].view(np.int8).reshape(m, inter),
+                          ref["qh"])
+    assert np.array_equal(y.view(np.uint32), ref["y"].view(np.uint32))
+    d = mats[2]
+    y64 = orc.gemv_f64(d.orc_packed(orc), d.scales, d.fmt, d.n, d.k, ref["qh"], ref["sh"])
+    assert rel_err(y, y64) <= TOL
+    return y
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("hidden,inter", [(256, 512), (384, 1152), (1024, 2816)])
+@pytest.mark.parametrize("m", [1, 2, 5, 8])
+def test_ffn_step_bit_exact(tq, orc, fmt, hidden, inter, m):
+    mats = ffn_mats(hidden, inter, fmt)
+    _check_ffn(tq, orc, mats, _acts(m, hidden, 0.01))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_ffn_full_size_layer_and_packed_rows(tq, orc, fmt):
+    """One full FFN layer (hidden 5120, intermediate 17408): m = 1 and the
+    packed m = 8 step against the oracle, and each packed row against its
+    single-row GPU run."""
+    import torch
+    hidden, inter = 5120, 17408
+    mats = ffn_mats(hidden, inter, fmt)
+    x8 = _acts(8, hidden, 0.01)
+    y1 = _check_ffn(tq, orc, mats, x8[:1])
+    y8 = _check_ffn(tq, orc, mats, x8)
+    assert np.array_equal(y8[0].view(np.uint32), y1[0].view(np.uint32))
+    for m in (2, 4):
+        ym, _ = _ffn_gpu(tq, mats, x8[:m])
+        assert np.array_equal(ym.view(np.uint32), y8[:m].view(np.uint32))
+    for r in range(1, 8):
+        yr, _ = _ffn_gpu(tq, mats, x8[r:r + 1])
+        assert np.array_equal(yr[0].view(np.uint32), y8[r].view(np.uint32)), r
+
+
+def test_ffn_repeat_runs_bit_identical(tq):
+    import torch
+    mats = ffn_mats(1024, 2816, 0)
+    x = _acts(4, 1024, 0.01)
+    first, _ = _ffn_gpu(tq, mats, x)
+    for _ in range(5):
+        again, _ = _ffn_gpu(tq, mats, x)
+        assert np.array_equal(again.view(np.uint32), first.view(np.uint32))
+
+
+def test_ffn_zero_activation(tq):
+    import torch
+    mats = ffn_mats(256, 512, 0)
+    y, _ = _ffn_gpu(tq, mats, np.zeros((2, 256), np.uint16))
+    assert np.all(y == 0)
+
+
+# ----------------------------------------------------------------------------
+# RMS-normalise and the layer stack
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,n", [(1, 5120), (8, 5120), (3, 300)])
+def test_rmsnorm_bit_exact(tq, orc, m, n):
+    import torch
+    rng = np.random.default_rng(3)
+    y = (rng.standard_normal((m, n)) * 7).astype(np.float32)
+    x = tq.rmsnorm_bf16(torch.from_numpy(y).cuda(), 1e-6)
+    assert np.array_equal(bf16_bits(x), orc.rmsnorm_bf16(y, 1e-6))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_stack_full_width(tq, orc, fmt):
+    """Three stacked full-width layers, rmsnorm between them, m = 1 and 2."""
+    import torch
+    hidden, inter, L = 5120, 17408, 3
+    layers = [ffn_mats(hidden, inter, fmt, layer=l) for l in range(L)]
+    x = _acts(2, hidden, 0.01)
+    xt = bf16_tensor(x)
+    for l, mats in enumerate(layers):
+        g, u, d = mats
+        y = tq.ffn_step(g.dev, u.dev, d.dev, xt)
+        if l + 1 < L:
+            xt = tq.rmsnorm_bf16(y, 1e-6)
+    torch.cuda.synchronize()
+    ref = orc.ffn_stack([(g.orc_packed(orc), g.scales, u.orc_packed(orc), u.scales,
+                          d.orc_packed(orc), d.scales) for g, u, d in layers],
+                        fmt, hidden, inter, x, 1e-6)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), ref.view(np.uint32))
