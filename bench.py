@@ -263,52 +263,80 @@ def run_ours(args, rank, world, local):
                           "tokens_per_s": round(m * 1e6 / us, 1),
                           "hbm_frac": round(lb / us / 1e3 / peak, 4)}
 
-    # --- roofline: the dominant kernel (fused gate/up GEMV), event-timed ---
+    # --- roofline: the dominant kernel (fused gate/up GEMV + h rotation) of the
+    #     step, launched through the stage entry points with events around it ---
     gu_bytes = gateup_bytes(HIDDEN, INTER, fmt)
-    q1, s1 = tq.rotate_quant(xs[1])
-    h1 = torch.empty((1, INTER), dtype=torch.bfloat16, device="cuda")
+    ws_r = tq.ffn_workspace(1, HIDDEN, INTER)
     n_gu = max(N_SETS, min(steps, 4000))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_gu)]
     for i in range(2 * N_SETS):
-        g, u, _ = layers[i % N_SETS]
-        tq.ffn_gateup(g, u, q1, s1, h=h1)
+        g, u, d = layers[i % N_SETS]
+        tq.ffn_stage_input(xs[1], INTER, ws_r)
+        tq.ffn_stage_gateup(g, u, 1, ws_r)
+        tq.ffn_stage_down(d, 1, ys[1], ws_r)
     torch.cuda.synchronize()
     for i, (e0, e1) in enumerate(evs):
-        g, u, _ = layers[i % N_SETS]
+        g, u, d = layers[i % N_SETS]
+        tq.ffn_stage_input(xs[1], INTER, ws_r)
         e0.record()
-        tq.ffn_gateup(g, u, q1, s1, h=h1)
+        tq.ffn_stage_gateup(g, u, 1, ws_r)
         e1.record()
+        tq.ffn_stage_down(d, 1, ys[1], ws_r)
     torch.cuda.synchronize()
     gu_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     gu_achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
 
-    # --- end to end through the public API with host buffers ---
+    # --- end to end through the public API with pinned host buffers: every step
+    #     copies x host->device, runs the step, copies y device->host.  The
+    #     per-step sequence is captured once as a CUDA graph and replayed. ---
     x_host = xs[1].cpu().pin_memory()
     y_host = torch.empty((1, HIDDEN), dtype=torch.float32).pin_memory()
     x_dev = torch.empty_like(xs[1])
-    e2e_steps = max(N_SETS, min(steps, 2000))
-    for i in range(N_SETS):
-        g, u, d = layers[i % N_SETS]
-        x_dev.copy_(x_host, non_blocking=True)
-        tq.ffn_step(g, u, d, x_dev, y=ys[1], workspace=wss[1])
-        y_host.copy_(ys[1], non_blocking=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(e2e_steps):
-        g, u, d = layers[i % N_SETS]
-        x_dev.copy_(x_host, non_blocking=True)
-        tq.ffn_step(g, u, d, x_dev, y=ys[1], workspace=wss[1])
-        y_host.copy_(ys[1], non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    wall_ms = (time.perf_counter() - t0) * 1e3
-    barrier(world)
-    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall_ms), world) / e2e_steps
+
+    def e2e_pass():
+        for g, u, d in layers:
+            x_dev.copy_(x_host, non_blocking=True)
+            tq.ffn_step(g, u, d, x_dev, y=ys[1], workspace=wss[1])
+            y_host.copy_(ys[1], non_blocking=True)
+
+    e2e_reps = max(1, min(reps, 4000 // N_SETS))
+    t_e2e, _ = time_graph(e2e_pass, e2e_reps, 2, world)
+    e2e_ms = max_over_ranks(t_e2e, world) / (e2e_reps * N_SETS)
     e2e_value = world * lb / (e2e_ms * 1e-3) / 1e9
+    # the same with one eager Python call per step (host launch overhead included)
+    for _ in range(2):
+        e2e_pass()
+    torch.cuda.synchronize()
+    eager_steps = N_SETS * max(1, min(reps, 1000 // N_SETS))
+    t0 = time.perf_counter()
+    for _ in range(eager_steps // N_SETS):
+        e2e_pass()
+    torch.cuda.synchronize()
+    eager_ms = (time.perf_counter() - t0) * 1e3 / eager_steps
+
+    # --- the 64-layer stacks (2-bit m = 1; 1-bit m = 1, 2, 4, 8) ---
+    stacks = {}
+    if not args.no_stack:
+        del layers
+        torch.cuda.empty_cache()
+        for sfmt, ms in ((0, (1,)), (1, (1, 2, 4, 8))):
+            stack_layers = make_weights(sfmt, 64, HIDDEN, INTER)
+            sb = 64 * layer_bytes(HIDDEN, INTER, sfmt)
+            for m in ms:
+                xm = synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
+                ym = torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda")
+                wsm = tq.ffn_workspace(m, HIDDEN, INTER)
+                t, _ = time_graph(lambda: tq.ffn_stack(stack_layers, xm, 1e-6, y=ym, workspace=wsm),
+                                  args.stack_reps, 2, world)
+                t = max_over_ranks(t, world)
+                us = t * 1e3 / args.stack_reps
+                stacks[f"{'ternary2' if sfmt == 0 else 'binary1'}_64L_m{m}"] = {
+                    "us_per_token_step": round(us, 2), "bytes_per_step": sb,
+                    "weight_gbs": round(sb / us / 1e3, 1), "hbm_frac": round(sb / us / 1e3 / peak, 4),
+                    "tokens_per_s": round(m * 1e6 / us, 1)}
+            del stack_layers
+            torch.cuda.empty_cache()
 
     result = {
         "metric": METRIC,
@@ -332,15 +360,19 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "hbm_frac": round(value / world / peak, 4),
         "sweep": sweep,
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<0,1,2> (fused gate/up + SiLU*up)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "gemv_kernel<0,1,true,2,2> (fused gate/up + SiLU*up + h rotation)",
                      "achieved": round(gu_achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gu_achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_ms * 1e3, 3),
                      "traffic": recorded_traffic("gateup_m1")},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
-                "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4},
-        "gpu_launches": steps * 4,
+                "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
+                "how": "pinned H2D copy + tq_ffn_step + D2H copy per step, graph-replayed",
+                "eager_us_per_step": round(eager_ms * 1e3, 3)},
+        "stack": stacks,
+        "gpu_launches": steps * 3,
         "clocks": clocks,
     }
     return result
@@ -380,6 +412,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--stack-reps", type=int, default=100)
+    ap.add_argument("--no-stack", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

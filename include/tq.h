@@ -29,7 +29,8 @@
  * Weight layout (the pages fix none; this library fixes this one):
  *   TQ_FMT_TERNARY2: 2-bit codes, 4 per byte.  Weight j of row i is in byte
  *     i*(k/4) + j/4 at bits 2*(j%4)..2*(j%4)+1, least significant first;
- *     code 0 -> 0, 1 -> +1, 2 -> -1 (3 must not occur; it reads as 0).
+ *     code 0 -> 0, 1 -> +1, 2 -> -1.  Code 3 must not occur (the kernels'
+ *     result for it is unspecified).
  *   TQ_FMT_BINARY1: 1 bit per weight, 8 per byte.  Weight j of row i is bit
  *     j%8 of byte i*(k/8) + j/8; 1 -> +1, 0 -> -1.
  *   scales: one IEEE fp16 per 128-weight block per row, [n][k/128].
@@ -122,8 +123,14 @@ tq_status tq_gemv(const tq_weight *w, const int8_t *q, const float *s, int32_t m
 tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t *qx,
                         const float *sx, int32_t m, uint16_t *h, tq_stream_t stream);
 
-/* Bytes of device workspace tq_ffn_step needs for these sizes. */
+/* Bytes of device workspace tq_ffn_step / tq_ffn_stack need for these sizes. */
 size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter);
+
+/* Zero-fill a workspace (an async memset on `stream`).  A workspace must be
+ * zero-filled once before its first use; every FFN call leaves it reusable.
+ * After a call that failed in flight (a CUDA error surfaced at
+ * synchronisation), initialise it again. */
+tq_status tq_ffn_workspace_init(void *workspace, size_t workspace_bytes, tq_stream_t stream);
 
 /* One decode FFN step for m packed rows:
  *   (qx, sx) = rotate_quant(x)                           [m][hidden]
@@ -138,10 +145,38 @@ size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter);
  * z < -103.972084045410156 gives 0.  Division is IEEE.
  * x: bf16 bits [m][hidden], 16-byte aligned.  y: fp32 [m][hidden].
  * workspace: >= tq_ffn_workspace_bytes(m, hidden, inter) bytes, 256-byte
- * aligned; its contents on entry do not matter and are garbage on exit. */
+ * aligned, initialised once by tq_ffn_workspace_init; it holds the step's
+ * intermediates (qx, sx, h, qh, sh) and the per-block completion counters of
+ * h, which every call leaves at zero.  Calls sharing a workspace must not run
+ * concurrently.
+ * The step runs as three kernels (rotate x; gate/up + SiLU*up, whose last CTA
+ * per 128-block of h rotates and quantises that block; down), each launched
+ * with programmatic stream serialisation: a kernel may start while earlier
+ * work in the stream drains, prefetching its weight matrices into L2, and
+ * reads nothing earlier work writes until that work has completed. */
 tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
                       const uint16_t *x, int32_t m, float *y, void *workspace,
                       size_t workspace_bytes, tq_stream_t stream);
+
+/* The three kernels of tq_ffn_step as separate calls on the same workspace
+ * (for timing a stage on its own): stage_input rotates and quantises x into
+ * the workspace; stage_gateup runs gate/up + SiLU*up and the rotation of h;
+ * stage_down writes y.  Issued in that order they compute tq_ffn_step. */
+tq_status tq_ffn_stage_input(const uint16_t *x, int32_t m, int32_t hidden, int32_t inter,
+                             void *workspace, size_t workspace_bytes, tq_stream_t stream);
+tq_status tq_ffn_stage_gateup(const tq_weight *gate, const tq_weight *up, int32_t m,
+                              void *workspace, size_t workspace_bytes, tq_stream_t stream);
+tq_status tq_ffn_stage_down(const tq_weight *down, int32_t m, float *y, void *workspace,
+                            size_t workspace_bytes, tq_stream_t stream);
+
+/* A stack of num_layers FFN layers for m packed rows: layer 0 reads x (bf16
+ * bits [m][hidden]); layer l > 0 reads rmsnorm_bf16(y_{l-1}, eps) (as
+ * tq_rmsnorm_bf16); y (fp32 [m][hidden]) receives the last layer's output.
+ * layers: 3 * num_layers weights, (gate, up, down) per layer, all of one
+ * format and shape.  Workspace as for tq_ffn_step. */
+tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16_t *x, int32_t m,
+                       float eps, float *y, void *workspace, size_t workspace_bytes,
+                       tq_stream_t stream);
 
 /* RMS-normalise (between stacked layers): for each row r,
  *   ss = sum_i y[r][i]^2 as 256 partial sums (partial t adds i = t, t+256, ...

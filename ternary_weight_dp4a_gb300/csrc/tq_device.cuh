@@ -28,7 +28,8 @@ __device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
 }
 
 // prmt.b32 in its default mode: byte i of the result is byte sel[4i+2:4i] of
-// the 8-byte pool {b:a}; sel bit 4i+3 must be 0 here (no sign replication).
+// the 8-byte pool {b:a}, or, when sel bit 4i+3 is set, that byte's sign bit
+// replicated over all eight bits.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -39,7 +40,118 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
-// 32-byte streaming load of weight codes (read once: no L1 allocation).
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while its predecessor in the stream still runs;
+// pdl_wait() blocks until that predecessor has completed and its writes are
+// visible (it returns at once when the launch had no such predecessor).
+// Nothing the predecessor writes may be read, and nothing it reads may be
+// written, before pdl_wait().
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Bulk prefetch of [p, p + bytes) from global memory into L2 (p 16-byte
+// aligned, bytes a multiple of 16).  Fire and forget: nothing waits on it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Prefetch the 16-byte-aligned interior of [p, p + bytes) into L2 in chunks
+// spread over the calling lanes (never touches a byte outside the range).
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes, int lane,
+                                                  int lanes) {
+    constexpr size_t kChunk = 16384;
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
+    for (uintptr_t a = a0 + static_cast<uintptr_t>(lane) * kChunk; a < a1;
+         a += static_cast<uintptr_t>(lanes) * kChunk) {
+        const uintptr_t n = a1 - a < kChunk ? a1 - a : kChunk;
+        prefetch_l2_bulk(reinterpret_cast<const void *>(a), static_cast<uint32_t>(n));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA engine) helpers.  Every wait is bounded by a
+// clock64 budget; a wait that runs out returns false and the caller records
+// an error instead of spinning forever.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// try_wait with a suspend-time hint: a waiting thread is parked by the
+// hardware (issuing nothing) until the phase completes or ~20 us pass, so
+// waiting warps do not take issue slots from warps that are computing.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
+// ~0.5 s at 2 GHz: far beyond any legitimate wait in these kernels
+constexpr long long kWaitBudgetCycles = 1ll << 30;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitBudgetCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy global -> shared (16-byte aligned addresses, size a multiple of
+// 16); completion is counted in bytes on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// 2D tensor copy global -> shared: the box at (x bytes, y rows) of the tensor
+// described by *tmap (a kernel-parameter tensor map) lands densely at dst;
+// completion is counted in bytes on `bar` (out-of-range parts read as zero).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Named barrier over the first `threads` threads of the CTA (id 1..15).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// 32-/16-byte streaming loads of weight codes (each byte is read once).
 struct u32x8 { uint32_t v[8]; };
 
 __device__ __forceinline__ u32x8 ldg_stream_32B(const void *p) {
@@ -63,6 +175,41 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint16_t *p) {
     uint16_t r;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
     return r;
+}
+
+// ---------------------------------------------------------------------------
+// 2-bit code decode.  Codes 0, 1, 2 (values 0, +1, -1) decode to the biased
+// bytes value + 1 = 1, 2, 0 with one prmt per four codes:
+//   even codes of a word (bits 4i..4i+1) as selectors w & 0x33333333 pick
+//   byte c of kTableA = {1, 2, 0, .};
+//   odd codes (bits 4i+2..4i+3) as selectors w & 0xcccccccc have nibble
+//   4*l + 8*h: l picks byte 0 of kTableA (1) or of kTableB (2), and h sets
+//   prmt's sign-replicate mode on byte 0 of kTableA (1 -> 0x00).
+// The bias is removed exactly per block: sum((w+1)*q) - sum(q).  A word's 16
+// codes come out as the dp4a operands for weights
+//   [0 2 4 6], [8 10 12 14], [1 3 5 7], [9 11 13 15]
+// which the staged activation matches.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kTableA = 0x00000201u;
+constexpr uint32_t kTableB = 0x00000002u;
+
+struct Decoded4 { uint32_t p[4]; };
+
+__device__ __forceinline__ Decoded4 decode_t2(uint32_t w) {
+    const uint32_t e = w & 0x33333333u;
+    const uint32_t o = w & 0xccccccccu;
+    Decoded4 d;
+    d.p[0] = prmt(kTableA, kTableB, e);
+    d.p[1] = prmt(kTableA, kTableB, e >> 16);
+    d.p[2] = prmt(kTableA, kTableB, o);
+    d.p[3] = prmt(kTableA, kTableB, o >> 16);
+    return d;
+}
+
+// Exact int -> float for |i| < 2^22 through the fp32 bit pattern of 2^23 + 2^22:
+// (float)(i + bias) where `magic_minus_bias` = 0x4b400000 - bias.
+__device__ __forceinline__ float int_to_float_exact(int i, int magic_minus_bias) {
+    return __fsub_rn(__int_as_float(i + magic_minus_bias), 12582912.0f);
 }
 
 // ---------------------------------------------------------------------------

@@ -2,7 +2,7 @@
 #include "tq_gemv_inst.cuh"
 
 namespace tq {
-cudaError_t launch_gemv_b1(const GemvArgs &a, int m, int nw, cudaStream_t stream) {
-    return dispatch_gemv<1>(a, m, nw, stream);
+cudaError_t launch_gemv_b1(const GemvArgs &a, int m, bool gateup, cudaStream_t stream) {
+    return dispatch_gemv<1>(a, m, gateup, stream);
 }
 }  // namespace tq

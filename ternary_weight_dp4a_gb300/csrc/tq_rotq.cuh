@@ -13,9 +13,8 @@
 
 namespace tq {
 
-// Lane l holds elements l, l+32, l+64, l+96 of one block in v[0..3].
-// Rotates in place and returns the quantisation scale; writes q via the
-// caller.  All 32 lanes must call.
+// Lane l holds elements l, l+32, l+64, l+96 of one block in v[0..3]; the block
+// is rotated in place.  All 32 lanes must call.
 __device__ __forceinline__ void wht128_warp(float v[4], int lane) {
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
@@ -43,8 +42,8 @@ __device__ __forceinline__ void wht128_warp(float v[4], int lane) {
     for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(v[i], c);
 }
 
-// Quantise a rotated block held as in wht128_warp.  Returns s; q[4] receive
-// the int8 codes of this lane's four elements.
+// Quantise a rotated block held as in wht128_warp: returns s, writes this
+// lane's four int8 codes to q[4].
 __device__ __forceinline__ float quant_block_warp(const float v[4], int8_t q[4]) {
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
@@ -65,29 +64,15 @@ __device__ __forceinline__ float quant_block_warp(const float v[4], int8_t q[4])
     return s;
 }
 
-// x: bf16 bits [m][k]; q: int8 [m][k]; s: fp32 [m][k/128].
-// One warp per (row, block); blockDim.x = 256.
-__global__ void __launch_bounds__(256) rotate_quant_kernel(const uint16_t *__restrict__ x,
-                                                           int64_t nblocks_total, int k,
-                                                           int8_t *__restrict__ q,
-                                                           float *__restrict__ s) {
-    const int lane = threadIdx.x & 31;
-    const int64_t gb = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (gb >= nblocks_total) return;
-    const int nb = k / kBlock;
-    const int64_t row = gb / nb;
-    const int b = static_cast<int>(gb % nb);
-    const uint16_t *xb = x + row * k + static_cast<int64_t>(b) * kBlock;
-    float v[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = bf16_bits_to_f32(xb[lane + 32 * c]);
+// Rotate + quantise one block whose four per-lane values are already loaded;
+// writes q (global layout) and s.
+__device__ __forceinline__ void rotq_block_store(float v[4], int lane, int8_t *qb, float *sb) {
     wht128_warp(v, lane);
     int8_t qq[4];
     const float sc = quant_block_warp(v, qq);
-    int8_t *qb = q + row * k + static_cast<int64_t>(b) * kBlock;
 #pragma unroll
     for (int c = 0; c < 4; ++c) qb[lane + 32 * c] = qq[c];
-    if (lane == 0) s[gb] = sc;
+    if (lane == 0) *sb = sc;
 }
 
 }  // namespace tq

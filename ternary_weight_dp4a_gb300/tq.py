@@ -23,8 +23,9 @@ MAX_ROWS = 8
 
 # every entry point include/tq.h declares
 EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",
-           "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_step",
-           "tq_rmsnorm_bf16")
+           "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_workspace_init",
+           "tq_ffn_step", "tq_ffn_stage_input", "tq_ffn_stage_gateup", "tq_ffn_stage_down",
+           "tq_ffn_stack", "tq_rmsnorm_bf16")
 
 _lock = threading.Lock()
 _lib = None
@@ -66,7 +67,12 @@ def load():
             L.tq_ffn_gateup.argtypes = [W, W, vp, vp, i32, vp, vp]
             L.tq_ffn_workspace_bytes.argtypes = [i32, i32, i32]
             L.tq_ffn_workspace_bytes.restype = sz
+            L.tq_ffn_workspace_init.argtypes = [vp, sz, vp]
             L.tq_ffn_step.argtypes = [W, W, W, vp, i32, vp, vp, sz, vp]
+            L.tq_ffn_stage_input.argtypes = [vp, i32, i32, i32, vp, sz, vp]
+            L.tq_ffn_stage_gateup.argtypes = [W, W, i32, vp, sz, vp]
+            L.tq_ffn_stage_down.argtypes = [W, i32, vp, vp, sz, vp]
+            L.tq_ffn_stack.argtypes = [W, i32, vp, i32, f32, vp, vp, sz, vp]
             L.tq_rmsnorm_bf16.argtypes = [vp, i32, i32, f32, vp, vp]
             for name in EXPORTS:
                 if name != "tq_status_string" and name != "tq_last_cuda_error" and \
@@ -167,8 +173,49 @@ def ffn_workspace_bytes(m: int, hidden: int, inter: int) -> int:
 
 
 def ffn_workspace(m: int, hidden: int, inter: int, device="cuda"):
+    """A zero-filled FFN workspace (zero is the state tq_ffn_workspace_init sets)."""
     import torch
-    return torch.empty(ffn_workspace_bytes(m, hidden, inter), dtype=torch.uint8, device=device)
+    return torch.zeros(ffn_workspace_bytes(m, hidden, inter), dtype=torch.uint8, device=device)
+
+
+def ffn_workspace_init(workspace, stream=None):
+    _check("tq_ffn_workspace_init", load().tq_ffn_workspace_init(
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ffn_stage_input(x, inter: int, workspace, stream=None):
+    m, hidden = x.shape
+    _check("tq_ffn_stage_input", load().tq_ffn_stage_input(
+        _ptr(x), m, hidden, inter, _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ffn_stage_gateup(gate: PackedWeight, up: PackedWeight, m: int, workspace, stream=None):
+    g, u = gate.c_struct(), up.c_struct()
+    _check("tq_ffn_stage_gateup", load().tq_ffn_stage_gateup(
+        ctypes.byref(g), ctypes.byref(u), m, _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ffn_stage_down(down: PackedWeight, m: int, y, workspace, stream=None):
+    d = down.c_struct()
+    _check("tq_ffn_stage_down", load().tq_ffn_stage_down(
+        ctypes.byref(d), m, _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ffn_stack(layers, x, eps: float = 1e-6, y=None, workspace=None, stream=None):
+    """layers: list of (gate, up, down) PackedWeight; x bf16 [m][hidden] ->
+    the last layer's y float32 [m][hidden]."""
+    import torch
+    m, hidden = x.shape
+    inter = layers[0][0].n
+    if y is None:
+        y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = ffn_workspace(m, hidden, inter, x.device)
+    arr = (_Weight * (3 * len(layers)))(*[w.c_struct() for layer in layers for w in layer])
+    _check("tq_ffn_stack", load().tq_ffn_stack(arr, len(layers), _ptr(x), m, eps, _ptr(y),
+                                               _ptr(workspace), workspace.numel(),
+                                               _stream(stream)))
+    return y
 
 
 def ffn_step(gate: PackedWeight, up: PackedWeight, down: PackedWeight, x, y=None,

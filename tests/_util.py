@@ -17,11 +17,12 @@ def round_up(x, a):
 
 def ws_offsets(m, hidden, inter):
     """Offsets of the FFN-step intermediates inside the workspace (qx, sx, h,
-    qh, sh), as tq_ffn_step lays them out; used only to read intermediates
-    back for stage-wise diagnosis."""
+    qh, sh, counters, ybuf), as tq_ffn_step lays them out; used only to read
+    intermediates back for stage-wise diagnosis."""
     off, o = 0, {}
     for name, nbytes in (("qx", m * hidden), ("sx", m * (hidden // B) * 4),
-                         ("h", m * inter * 2), ("qh", m * inter), ("sh", m * (inter // B) * 4)):
+                         ("h", m * inter * 2), ("qh", m * inter), ("sh", m * (inter // B) * 4),
+                         ("counters", (inter // B) * 4), ("ybuf", m * hidden * 4), ("err", 4)):
         o[name] = off
         off = round_up(off + nbytes, 256)
     o["total"] = off
@@ -62,6 +63,18 @@ def bf16_tensor(bits_np):
 def bf16_bits(t):
     import torch
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def fold_rel_err(y, ref64, orc, packed, scales, fmt, n, k, q, s):
+    """max |y - ref| / sum_b |t_b|: the error relative to the magnitude of the
+    block terms being summed (t_b = d_b * sw * s), which stays meaningful for
+    outputs whose terms cancel."""
+    d = orc.blockdots(packed, fmt, n, k, q).astype(np.float64)          # [m][n][nb]
+    sw = np.asarray(scales, np.float16).astype(np.float64)               # [n][nb]
+    sa = np.asarray(s, np.float64).reshape(d.shape[0], 1, -1)            # [m][1][nb]
+    mag = (np.abs(d) * sw[None] * sa).sum(axis=2)
+    err = np.abs(np.asarray(y, np.float64) - ref64)
+    return float((err / np.maximum(mag, 1e-30)).max()) if err.size else 0.0
 
 
 def rel_err(y, ref):

@@ -40,8 +40,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # qx 5120 | sx 160->256 | h 34816 | qh 17408 | sh 544->768, each 256-aligned
-    assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == 5120 + 256 + 34816 + 17408 + 768
+    # qx 5120 | sx 160->256 | h 34816 | qh 17408 | sh 544->768 | counters 544->768 |
+    # ybuf 20480 | err 4->256, each 256-aligned
+    assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == \
+        5120 + 256 + 34816 + 17408 + 768 + 768 + 20480 + 256
     assert lib.tq_ffn_workspace_bytes(0, 5120, 17408) == 0
 
 
@@ -87,6 +89,14 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.tq_rotate_quant(p, 0, 128, p, p, st) == 1
     assert lib.tq_rotate_quant(p, 1, 130, p, p, st) == 1
     assert lib.tq_rmsnorm_bf16(None, 1, 128, ctypes.c_float(1e-6), p, st) == 1
+    assert lib.tq_ffn_workspace_init(None, 16, st) == 1
+    assert lib.tq_ffn_stage_input(p, 1, 256, 512, None, 4096, st) == 1
+    assert lib.tq_ffn_stage_input(p, 9, 256, 512, p, 1 << 20, st) == 1
+    big = ctypes.c_void_p(0x100000)
+    assert lib.tq_ffn_stage_input(p, 1, 256, 512, big, 16, st) == 4
+    assert lib.tq_ffn_stack(None, 1, p, 1, ctypes.c_float(1e-6), p, big, 1 << 20, st) == 1
+    w = (tq._Weight * 3)(_w(n=512, k=256), _w(n=512, k=256), _w(n=256, k=512))
+    assert lib.tq_ffn_stack(w, 0, p, 1, ctypes.c_float(1e-6), p, big, 1 << 20, st) == 1
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

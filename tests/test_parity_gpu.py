@@ -2,14 +2,15 @@
 
 Bars (per the method's exactness): int8 codes, fp32 activation scales and int32
 block dots bit-exact; fp32 outputs bit-exact against the oracle's documented
-fold order and within max relative error 1e-4 of the fp64 definition; every
+fold order, and within relative error 1e-4 of the fp64 definition, measured
+against the summed magnitude of each output's block terms; every
 row of a packed step bit-identical to its single-row run; repeated runs
 bit-identical.
 """
 import numpy as np
 import pytest
 
-from _util import Mat, bf16_bits, bf16_tensor, ffn_mats, rel_err, ws_offsets
+from _util import Mat, bf16_bits, bf16_tensor, ffn_mats, fold_rel_err, ws_offsets
 from ternary_weight_dp4a_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -79,7 +80,8 @@ def test_gemv_bit_exact(tq, orc, fmt, n, k, m):
     y_ref = orc.gemv(packed, w.scales, fmt, n, k, q_ref, s_ref)
     yg = y.cpu().numpy()
     assert np.array_equal(yg.view(np.uint32), y_ref.view(np.uint32))
-    assert rel_err(yg, orc.gemv_f64(packed, w.scales, fmt, n, k, q_ref, s_ref)) <= TOL
+    y64 = orc.gemv_f64(packed, w.scales, fmt, n, k, q_ref, s_ref)
+    assert fold_rel_err(yg, y64, orc, packed, w.scales, fmt, n, k, q_ref, s_ref) <= TOL
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
@@ -151,7 +153,8 @@ def _check_ffn(tq, orc, mats, x_bits):
     assert np.array_equal(y.view(np.uint32), ref["y"].view(np.uint32))
     d = mats[2]
     y64 = orc.gemv_f64(d.orc_packed(orc), d.scales, d.fmt, d.n, d.k, ref["qh"], ref["sh"])
-    assert rel_err(y, y64) <= TOL
+    assert fold_rel_err(y, y64, orc, d.orc_packed(orc), d.scales, d.fmt, d.n, d.k,
+                        ref["qh"], ref["sh"]) <= TOL
     return y
 
 
@@ -181,6 +184,42 @@ def test_ffn_full_size_layer_and_packed_rows(tq, orc, fmt):
     for r in range(1, 8):
         yr, _ = _ffn_gpu(tq, mats, x8[r:r + 1])
         assert np.array_equal(yr[0].view(np.uint32), y8[r].view(np.uint32)), r
+
+
+def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
+    """The per-block completion counters are zero after every step, and the three
+    stage calls on one workspace compute exactly the step."""
+    import torch
+    hidden, inter, m = 1024, 2816, 3
+    mats = ffn_mats(hidden, inter, 0)
+    x = _acts(m, hidden, 0.01)
+    y_step, ws = _ffn_gpu(tq, mats, x)
+    o = ws_offsets(m, hidden, inter)
+    wsn = ws.cpu().numpy()
+    cnt = wsn[o["counters"]:o["counters"] + 4 * (inter // 128)].view(np.uint32)
+    assert np.all(cnt == 0)
+    assert wsn[o["err"]:o["err"] + 4].view(np.uint32)[0] == 0     # no wait ran out
+    g, u, d = mats
+    ws2 = tq.ffn_workspace(m, hidden, inter)
+    y2 = torch.empty((m, hidden), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        tq.ffn_stage_input(bf16_tensor(x), inter, ws2)
+        tq.ffn_stage_gateup(g.dev, u.dev, m, ws2)
+        tq.ffn_stage_down(d.dev, m, y2, ws2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y2.cpu().numpy().view(np.uint32), y_step.view(np.uint32))
+
+
+def test_ffn_gateup_standalone_matches_oracle(tq, orc):
+    import torch
+    hidden, inter, m = 1024, 2816, 2
+    g, u, _ = ffn_mats(hidden, inter, 0)
+    x = _acts(m, hidden, 0.01)
+    qx, sx = orc.rotate_quant(x)
+    h = tq.ffn_gateup(g.dev, u.dev, torch.from_numpy(qx).cuda(), torch.from_numpy(sx).cuda())
+    gref = orc.gemv(g.orc_packed(orc), g.scales, 0, inter, hidden, qx, sx)
+    uref = orc.gemv(u.orc_packed(orc), u.scales, 0, inter, hidden, qx, sx)
+    assert np.array_equal(bf16_bits(h), orc.silu_mul_bf16(gref, uref))
 
 
 def test_ffn_repeat_runs_bit_identical(tq):
@@ -226,8 +265,16 @@ def test_stack_full_width(tq, orc, fmt):
         y = tq.ffn_step(g.dev, u.dev, d.dev, xt)
         if l + 1 < L:
             xt = tq.rmsnorm_bf16(y, 1e-6)
+    # the fused stack entry point (norm + rotation kernel between layers)
+    ys = tq.ffn_stack([(g.dev, u.dev, d.dev) for g, u, d in layers], bf16_tensor(x), 1e-6)
     torch.cuda.synchronize()
     ref = orc.ffn_stack([(g.orc_packed(orc), g.scales, u.orc_packed(orc), u.scales,
                           d.orc_packed(orc), d.scales) for g, u, d in layers],
                         fmt, hidden, inter, x, 1e-6)
     assert np.array_equal(y.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert np.array_equal(ys.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # each packed row equals its single-row stack
+    for r in range(2):
+        yr = tq.ffn_stack([(g.dev, u.dev, d.dev) for g, u, d in layers],
+                          bf16_tensor(x[r:r + 1]), 1e-6)
+        assert torch.equal(yr[0].view(torch.int32), ys[r].view(torch.int32))
