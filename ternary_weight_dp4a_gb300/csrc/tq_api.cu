@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "tq.h"
+#include "tq_fused_launch.h"
 #include "tq_launch.h"
 #include "tq_misc.cuh"
 #include "tq_norm_kernels.cuh"
@@ -30,9 +31,10 @@ constexpr size_t kWsAlign = 256;
 // Workspace of the FFN step / stack, each section 256-byte aligned:
 //   qx int8 [m][hidden] | sx f32 [m][hidden/128] | h bf16 [m][inter] |
 //   qh int8 [m][inter]  | sh f32 [m][inter/128]  | counters u32 [inter/128] |
-//   ybuf f32 [m][hidden] | err u32 (nonzero: a kernel's bounded wait ran out)
+//   ybuf f32 [m][hidden] | err u32 (nonzero: a kernel's bounded wait ran out) |
+//   gbar u32[2] (grid barrier of the fused kernel)
 struct FfnWorkspace {
-    size_t qx, sx, h, qh, sh, counters, ybuf, err, total;
+    size_t qx, sx, h, qh, sh, counters, ybuf, err, gbar, total;
 };
 
 FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
@@ -46,6 +48,7 @@ FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
     w.counters = off; off = round_up(off + static_cast<size_t>(inter / 128) * 4, kWsAlign);
     w.ybuf = off; off = round_up(off + static_cast<size_t>(m * hidden) * 4, kWsAlign);
     w.err = off; off = round_up(off + 4, kWsAlign);
+    w.gbar = off; off = round_up(off + 8, kWsAlign);
     w.total = off;
     return w;
 }
@@ -59,6 +62,7 @@ struct FfnPtrs {
     unsigned *counters;
     float *ybuf;
     unsigned *err;
+    unsigned *gbar;
 };
 
 FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
@@ -66,7 +70,8 @@ FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
     return FfnPtrs{reinterpret_cast<int8_t *>(b + L.qx), reinterpret_cast<float *>(b + L.sx),
                    reinterpret_cast<uint16_t *>(b + L.h), reinterpret_cast<int8_t *>(b + L.qh),
                    reinterpret_cast<float *>(b + L.sh), reinterpret_cast<unsigned *>(b + L.counters),
-                   reinterpret_cast<float *>(b + L.ybuf), reinterpret_cast<unsigned *>(b + L.err)};
+                   reinterpret_cast<float *>(b + L.ybuf), reinterpret_cast<unsigned *>(b + L.err),
+                   reinterpret_cast<unsigned *>(b + L.gbar)};
 }
 
 tq_status check_weight(const tq_weight *w) {
@@ -159,6 +164,38 @@ cudaError_t launch_down(const tq_weight *down, const int8_t *qh, const float *sh
     dn.y = y;
     dn.err = err;
     return launch_gemv(dn, down->fmt, m, false, stream);
+}
+
+bool use_fused(int fmt, int m, int hidden, int inter) {
+    if (!tq::fused_supported(fmt, m, hidden, inter)) return false;
+    cudaError_t e = cudaSuccess;
+    const size_t have = tq::max_smem_optin(&e);
+    return e == cudaSuccess && tq::fused_smem(fmt, m, hidden, inter) + 1024 <= have;
+}
+
+tq::FfnFusedArgs fused_args(const FfnPtrs &P, int hidden, int inter, float eps) {
+    tq::FfnFusedArgs f{};
+    f.hidden = hidden;
+    f.inter = inter;
+    f.eps = eps;
+    f.ybuf = P.ybuf;
+    f.qx = P.qx;
+    f.sx = P.sx;
+    f.h = P.h;
+    f.qh = P.qh;
+    f.sh = P.sh;
+    f.counters = P.counters;
+    f.gbar = P.gbar;
+    f.err = P.err;
+    return f;
+}
+
+void set_layer(tq::FfnFusedArgs &f, int i, const tq_weight *g, const tq_weight *u, const tq_weight *d) {
+    const tq_weight *w[3] = {g, u, d};
+    for (int j = 0; j < 3; ++j) {
+        f.layer[i].codes[j] = w[j]->codes;
+        f.layer[i].scales[j] = w[j]->scales;
+    }
 }
 
 }  // namespace
@@ -312,6 +349,14 @@ tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weigh
     if ((st = check_ffn_smem(gate->fmt, m, hidden, inter)) != TQ_OK) return st;
     const FfnPtrs P = ffn_ptrs(workspace, ffn_layout(m, hidden, inter));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (use_fused(gate->fmt, m, hidden, inter)) {
+        tq::FfnFusedArgs f = fused_args(P, hidden, inter, 0.0f);
+        f.num_layers = 1;
+        f.x = x;
+        f.y = y;
+        set_layer(f, 0, gate, up, down);
+        return cuda_status(tq::launch_ffn_fused(f, gate->fmt, m, s));
+    }
     cudaError_t e = launch_rotq(x, m, hidden, P.qx, P.sx, s);
     if (e == cudaSuccess)
         e = launch_gateup(gate, up, P.qx, P.sx, m, P.h, P.qh, P.sh, P.counters, P.err, s);
@@ -336,6 +381,24 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
     if ((st = check_ffn_smem(layers[0].fmt, m, hidden, inter)) != TQ_OK) return st;
     const FfnPtrs P = ffn_ptrs(workspace, ffn_layout(m, hidden, inter));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (use_fused(layers[0].fmt, m, hidden, inter)) {
+        // chunks of up to kFusedMaxLayers layers per launch; a chunk after the
+        // first starts from the RMS-normalised output of the one before
+        cudaError_t e = cudaSuccess;
+        for (int l0 = 0; l0 < num_layers && e == cudaSuccess; l0 += tq::kFusedMaxLayers) {
+            const int cnt = num_layers - l0 < tq::kFusedMaxLayers ? num_layers - l0 : tq::kFusedMaxLayers;
+            tq::FfnFusedArgs f = fused_args(P, hidden, inter, eps);
+            f.num_layers = cnt;
+            f.input_is_y = l0 > 0;
+            f.x = x;
+            f.y_in = P.ybuf;
+            f.y = l0 + cnt == num_layers ? y : P.ybuf;
+            for (int i = 0; i < cnt; ++i)
+                set_layer(f, i, &layers[3 * (l0 + i)], &layers[3 * (l0 + i) + 1], &layers[3 * (l0 + i) + 2]);
+            e = tq::launch_ffn_fused(f, layers[0].fmt, m, s);
+        }
+        return cuda_status(e);
+    }
     cudaError_t e = launch_rotq(x, m, hidden, P.qx, P.sx, s);
     for (int l = 0; l < num_layers && e == cudaSuccess; ++l) {
         const tq_weight *L = &layers[3 * l];

@@ -158,8 +158,10 @@ def _check_ffn(tq, orc, mats, x_bits):
     return y
 
 
+# (1024, 3072) and (2048, 4096) take the fused single-kernel path at m <= 2
 @pytest.mark.parametrize("fmt", [0, 1])
-@pytest.mark.parametrize("hidden,inter", [(256, 512), (384, 1152), (1024, 2816)])
+@pytest.mark.parametrize("hidden,inter", [(256, 512), (384, 1152), (1024, 2816), (1024, 3072),
+                                          (2048, 4096)])
 @pytest.mark.parametrize("m", [1, 2, 5, 8])
 def test_ffn_step_bit_exact(tq, orc, fmt, hidden, inter, m):
     mats = ffn_mats(hidden, inter, fmt)
@@ -188,9 +190,10 @@ def test_ffn_full_size_layer_and_packed_rows(tq, orc, fmt):
 
 def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
     """The per-block completion counters are zero after every step, and the three
-    stage calls on one workspace compute exactly the step."""
+    stage calls (the three-kernel path) compute exactly the step (the fused
+    single-kernel path at m <= 2)."""
     import torch
-    hidden, inter, m = 1024, 2816, 3
+    hidden, inter, m = 1024, 3072, 2
     mats = ffn_mats(hidden, inter, 0)
     x = _acts(m, hidden, 0.01)
     y_step, ws = _ffn_gpu(tq, mats, x)
@@ -199,6 +202,7 @@ def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
     cnt = wsn[o["counters"]:o["counters"] + 4 * (inter // 128)].view(np.uint32)
     assert np.all(cnt == 0)
     assert wsn[o["err"]:o["err"] + 4].view(np.uint32)[0] == 0     # no wait ran out
+    assert wsn[o["gbar"]:o["gbar"] + 4].view(np.uint32)[0] == 0   # grid barrier count reset
     g, u, d = mats
     ws2 = tq.ffn_workspace(m, hidden, inter)
     y2 = torch.empty((m, hidden), dtype=torch.float32, device="cuda")
