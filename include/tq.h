@@ -178,6 +178,39 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
                        float eps, float *y, void *workspace, size_t workspace_bytes,
                        tq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * FFN step without a caller-supplied workspace.  (The pages have no
+ * counterpart to this entry point: it exists for callers, not for the method.)
+ *
+ * Some callers cannot allocate device memory at the point where they run the
+ * step: a plugin inside a host application that owns every device allocation
+ * and offers no allocator, or a real-time loop whose rules forbid calling the
+ * allocator after start-up.  tq_ffn_step_static serves them: it computes
+ * exactly what tq_ffn_step computes, with its scratch in a fixed array of
+ * tq_ffn_static_workspace_bytes() bytes (about 1.1 MB) that is part of the
+ * library.  Every GPU that loads the library holds one such array until the
+ * process exits.  The call allocates nothing (no cudaMalloc, no cudaFree).
+ *
+ * Limits: m <= TQ_STATIC_MAX_ROWS, hidden <= TQ_STATIC_MAX_HIDDEN,
+ * intermediate <= TQ_STATIC_MAX_INTER; larger sizes return
+ * TQ_ERR_UNSUPPORTED before anything is launched.
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress); make that first call before beginning any
+ * stream capture.  Each call then zero-fills the part of the array it uses
+ * with an asynchronous memset on `stream` before launching the step.
+ * All calls on a device share the one array: calls whose work can overlap on
+ * the GPU (different streams without ordering between them) race on it and
+ * must not be issued. */
+#define TQ_STATIC_MAX_ROWS 8
+#define TQ_STATIC_MAX_HIDDEN 8192
+#define TQ_STATIC_MAX_INTER 32768
+
+size_t tq_ffn_static_workspace_bytes(void);
+
+tq_status tq_ffn_step_static(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
+                             const uint16_t *x, int32_t m, float *y, tq_stream_t stream);
+
 /* RMS-normalise (between stacked layers): for each row r,
  *   ss = sum_i y[r][i]^2 as 256 partial sums (partial t adds i = t, t+256, ...
  *        in ascending order from +0.0) combined pairwise at distance

@@ -201,6 +201,9 @@ void set_layer(tq::FfnFusedArgs &f, int i, const tq_weight *g, const tq_weight *
 }  // namespace
 
 namespace tq {
+// lets other translation units report through tq_last_cuda_error()
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+
 size_t max_smem_optin(cudaError_t *err) {
     int dev = 0, v = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -25,7 +25,8 @@ MAX_ROWS = 8
 EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",
            "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_workspace_init",
            "tq_ffn_step", "tq_ffn_stage_input", "tq_ffn_stage_gateup", "tq_ffn_stage_down",
-           "tq_ffn_stack", "tq_rmsnorm_bf16")
+           "tq_ffn_stack", "tq_ffn_static_workspace_bytes", "tq_ffn_step_static",
+           "tq_rmsnorm_bf16")
 
 _lock = threading.Lock()
 _lib = None
@@ -74,9 +75,12 @@ def load():
             L.tq_ffn_stage_down.argtypes = [W, i32, vp, vp, sz, vp]
             L.tq_ffn_stack.argtypes = [W, i32, vp, i32, f32, vp, vp, sz, vp]
             L.tq_rmsnorm_bf16.argtypes = [vp, i32, i32, f32, vp, vp]
+            L.tq_ffn_static_workspace_bytes.argtypes = []
+            L.tq_ffn_static_workspace_bytes.restype = sz
+            L.tq_ffn_step_static.argtypes = [W, W, W, vp, i32, vp, vp]
             for name in EXPORTS:
-                if name != "tq_status_string" and name != "tq_last_cuda_error" and \
-                        name != "tq_ffn_workspace_bytes":
+                if name not in ("tq_status_string", "tq_last_cuda_error", "tq_ffn_workspace_bytes",
+                                "tq_ffn_static_workspace_bytes"):
                     getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -231,6 +235,20 @@ def ffn_step(gate: PackedWeight, up: PackedWeight, down: PackedWeight, x, y=None
     _check("tq_ffn_step", load().tq_ffn_step(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d),
                                              _ptr(x), m, _ptr(y), _ptr(workspace),
                                              workspace.numel(), _stream(stream)))
+    return y
+
+
+def ffn_step_static(gate: PackedWeight, up: PackedWeight, down: PackedWeight, x, y=None,
+                    stream=None):
+    """The FFN step with the library's built-in scratch (no workspace argument;
+    see tq_ffn_step_static in include/tq.h for who needs it and its limits)."""
+    import torch
+    m, hidden = x.shape
+    if y is None:
+        y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
+    g, u, d = gate.c_struct(), up.c_struct(), down.c_struct()
+    _check("tq_ffn_step_static", load().tq_ffn_step_static(
+        ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), _ptr(x), m, _ptr(y), _stream(stream)))
     return y
 
 

@@ -1,0 +1,57 @@
+"""tq_ffn_step_static: the FFN step for callers that cannot allocate device
+memory when they run it (a plugin whose host application owns every device
+allocation, a real-time loop that may not call the allocator after start-up).
+Its scratch is an array built into the library instead of a caller-supplied
+workspace.  It must give exactly the bits tq_ffn_step gives with a
+caller-owned workspace, call after call, and refuse sizes beyond the array.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes on its own in a fresh process.
+"""
+import ctypes
+
+import pytest
+
+from _util import bf16_tensor, ffn_mats
+from ternary_weight_dp4a_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ternary_weight_dp4a_gb300 import build, tq as tqmod
+    build.build()
+    tqmod.load()
+    return tqmod
+
+
+# (1024, 3072, 1) runs the fused single-kernel step, (1024, 2816, 3) the
+# three-kernel step
+@pytest.mark.parametrize("hidden,inter,m", [(1024, 3072, 1), (1024, 2816, 3)])
+def test_static_scratch_step_matches_workspace_step(tq, hidden, inter, m):
+    import torch
+    g, u, d = (w.dev for w in ffn_mats(hidden, inter, 0))
+    for call in range(2):          # two calls in a row share the built-in scratch
+        x = bf16_tensor(synth.activation(m, hidden, seed=synth.SEED_ACT_BASE + 100 * call,
+                                         outlier_frac=0.01))
+        y_static = tq.ffn_step_static(g, u, d, x)
+        y_ref = tq.ffn_step(g, u, d, x)
+        torch.cuda.synchronize()
+        assert torch.equal(y_static.view(torch.int32), y_ref.view(torch.int32)), call
+
+
+def test_static_scratch_refuses_sizes_beyond_its_limit(tq):
+    lib = tq.load()
+    assert lib.tq_ffn_static_workspace_bytes() >= lib.tq_ffn_workspace_bytes(8, 8192, 32768)
+    # shapes only: nothing is read when the call refuses
+    big = dict(hidden=8192 + 1024, inter=17408)
+    g = tq._Weight(0x1000, 0x2000, big["inter"], big["hidden"], 0)
+    u = tq._Weight(0x3000, 0x4000, big["inter"], big["hidden"], 0)
+    d = tq._Weight(0x5000, 0x6000, big["hidden"], big["inter"], 0)
+    p = ctypes.c_void_p(0x7000)
+    st = lib.tq_ffn_step_static(ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), p, 1, p,
+                                ctypes.c_void_p(0))
+    assert st == 3                 # TQ_ERR_UNSUPPORTED
