@@ -106,8 +106,11 @@ tq_status tq_rotate_quant(const uint16_t *x, int32_t m, int32_t k, int8_t *q, fl
  * Summary).  For row r and output i:
  *   d_b = sum_{j in block b} W[i][j] * q[r][j]          (exact int32)
  *   t_b = (float)d_b * (fp16->fp32(scales[i][b]) * s[r][b])
- *   y[r][i] = ((P0+P1)+(P2+P3)) + ((P4+P5)+(P6+P7)),
- *   P_p = (((0 + t_p) + t_{p+8}) + t_{p+16}) + ...      (fp32, ascending b)
+ *   S_j = (((0 + t_{8j}) + t_{8j+1}) + ...) + t_{min(8j+7, nb-1)}
+ *                                       (fp32, segments of 8 consecutive blocks)
+ *   y[r][i] = pairwise tree over S_0 .. S_{nseg-1}: each level adds nodes
+ *             (0,1), (2,3), ... in order and passes an odd last node up,
+ *             until one value remains,
  * which is the same for every m, so each row of a packed step is
  * bit-identical to its single-row result.
  * q: int8 [m][k] (16-byte aligned); s: fp32 [m][k/128]; y: fp32 [m][n].

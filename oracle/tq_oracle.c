@@ -18,7 +18,7 @@
  *      an exact int32 dot of the int8 activation with the {-1,0,+1} weights,
  *      scaled by the block's fp16 weight scale and the activation block's
  *      fp32 scale, accumulated in fp32 in a fixed documented order
- *      (same PR, Summary: "dp4a GEMV", "per-block fold and shuffle tree").
+ *      (same PR: "dp4a GEMV"; "lane walk, per-block fold and shuffle tree").
  *   3. h = bf16(SiLU(gate) * up).
  *   4. h is rotated and quantised like x, then the down GEMV gives y (fp32).
  *   5. (stack only) x_next = bf16(RMS-normalise(y)).
@@ -222,27 +222,40 @@ void orc_blockdots(const uint8_t *packed, int fmt, int n, int k,
 
 /* The documented fp32 fold and reduction of one output.
  * Per block: t_b = (float)dot_b * (fp32(sw[n,b]) * s[r,b])  (two roundings,
- * that association).  Eight partial sums: partial p adds t_b for
- * b = p, p+8, p+16, ... in ascending order, starting from +0.0f.  The eight
- * partials then combine as ((p0+p1)+(p2+p3)) + ((p4+p5)+(p6+p7)).
- * Reading taken for "per-block fold and shuffle tree" (PR #1154 commit
- * message) and "accumulated in fp32 in a fixed block order"; the order does
- * not depend on how many rows share the step. */
+ * that association).  Lane walk: the blocks split into segments of eight
+ * consecutive blocks (the last one shorter when nb is not a multiple of 8);
+ * segment j adds t_b for b = 8j, 8j+1, ... in ascending order starting from
+ * +0.0f.  Shuffle tree: the segment sums combine pairwise, level by level --
+ * node i of the next level is left + right of nodes 2i and 2i+1, and an odd
+ * last node passes up unchanged -- until one value remains.
+ * Reading taken for "each row's lane walk, per-block fold and shuffle tree"
+ * (PR #1154 commit message): the pages fix no lane count or block order, so
+ * the walk is taken over consecutive blocks; the order does not depend on
+ * how many rows share the step. */
+#define ORC_SEG 8
 static float fold_output(const int32_t *dots_nb, const uint16_t *sw_row,
                          const float *s_row, int nb) {
-    float part[8];
-    for (int p = 0; p < 8; p++) {
+    int nseg = (nb + ORC_SEG - 1) / ORC_SEG;
+    float *node = (float *)malloc(sizeof(float) * (size_t)nseg);
+    for (int j = 0; j < nseg; j++) {
         float acc = 0.0f;
-        for (int b = p; b < nb; b += 8) {
+        for (int b = j * ORC_SEG; b < nb && b < (j + 1) * ORC_SEG; b++) {
             float ws = orc_f16_to_f32(sw_row[b]) * s_row[b];
             float t = (float)dots_nb[b] * ws;
             acc = acc + t;
         }
-        part[p] = acc;
+        node[j] = acc;
     }
-    float a01 = part[0] + part[1], a23 = part[2] + part[3];
-    float a45 = part[4] + part[5], a67 = part[6] + part[7];
-    return (a01 + a23) + (a45 + a67);
+    int cnt = nseg;
+    while (cnt > 1) {
+        int next = 0;
+        for (int i = 0; i + 1 < cnt; i += 2) node[next++] = node[i] + node[i + 1];
+        if (cnt % 2 == 1) node[next++] = node[cnt - 1];
+        cnt = next;
+    }
+    float y = node[0];
+    free(node);
+    return y;
 }
 
 /* y: fp32 [m][n].  scales: fp16 bits [n][k/128]. */

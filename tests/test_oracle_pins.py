@@ -462,9 +462,31 @@ def test_mutants_are_rejected(orc):
     good = np.einsum("nbk,bk,nb,b->n", Wd, qq.astype(np.float64).reshape(2, B),
                      sw.astype(np.float64), ss[0].astype(np.float64))
     assert np.abs(y_mut[0] - good).max() > 1e-3 * np.abs(good).max()
-    # a sequential fold gives 2 on the fold-order worked example, not the documented 1
-    t = [2.0 ** 24, 1.0, -(2.0 ** 24), 1.0] + [0.0] * 4 + [1.0] + [0.0] * 7
-    acc = np.float32(0)
+    # other fold orders give other values on the fold-order worked example,
+    # so the golden pin rejects each of them
+    g = _golden("fold_order.txt")
+    t = [np.float32(int(d)) * np.float32(float(sv)) for d, sv in zip(g["dots"], g["act_scales"])]
+    want = np.float32(float(g["expected_fp32"][0]))
+    acc = np.float32(0)                                  # one sequential walk over all blocks
     for v in t:
-        acc = np.float32(acc + np.float32(v))
-    assert acc == np.float32(2.0)
+        acc = np.float32(acc + v)
+    assert acc == np.float32(float(g["expected_sequential_blocks"][0])) and acc != want
+    segs = []                                            # segment sums, then a sequential combine
+    for j in range(0, len(t), 8):
+        a = np.float32(0)
+        for v in t[j:j + 8]:
+            a = np.float32(a + v)
+        segs.append(a)
+    acc = np.float32(0)
+    for v in segs:
+        acc = np.float32(acc + v)
+    assert acc == np.float32(float(g["expected_sequential_segments"][0])) and acc != want
+    parts = []                                           # eight strided chains and a fixed tree
+    for p in range(8):
+        a = np.float32(0)
+        for v in t[p::8]:
+            a = np.float32(a + v)
+        parts.append(a)
+    old = np.float32(np.float32(np.float32(parts[0] + parts[1]) + np.float32(parts[2] + parts[3]))
+                     + np.float32(np.float32(parts[4] + parts[5]) + np.float32(parts[6] + parts[7])))
+    assert old == np.float32(2.0) and old != want
