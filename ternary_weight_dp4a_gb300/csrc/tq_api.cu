@@ -7,7 +7,8 @@
 #include <cuda_runtime.h>
 
 #include "tq.h"
-#include "tq_fused_launch.h"
+#include "tq_kernel.cuh"
+#include "tq_kernel_launch.h"
 #include "tq_launch.h"
 #include "tq_misc.cuh"
 #include "tq_norm_kernels.cuh"
@@ -32,9 +33,12 @@ constexpr size_t kWsAlign = 256;
 //   qx int8 [m][hidden] | sx f32 [m][hidden/128] | h bf16 [m][inter] |
 //   qh int8 [m][inter]  | sh f32 [m][inter/128]  | counters u32 [inter/128] |
 //   ybuf f32 [m][hidden] | err u32 (nonzero: a kernel's bounded wait ran out) |
-//   gbar u32[2] (grid barrier of the fused kernel)
+//   gbar u64 (grid-barrier arrivals of the step kernel; only ever grows) |
+//   hst i8 [m*inter] (h quantised again, staged as the down phase reads it:
+//   per pass of rows r0.., [inter/128][rows][128] permuted) |
+//   hsn (f32 scale, i32 0x4b400000 - sum q) [m][inter/128]
 struct FfnWorkspace {
-    size_t qx, sx, h, qh, sh, counters, ybuf, err, gbar, total;
+    size_t qx, sx, h, qh, sh, counters, ybuf, err, gbar, hst, hsn, total;
 };
 
 FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
@@ -49,6 +53,8 @@ FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
     w.ybuf = off; off = round_up(off + static_cast<size_t>(m * hidden) * 4, kWsAlign);
     w.err = off; off = round_up(off + 4, kWsAlign);
     w.gbar = off; off = round_up(off + 8, kWsAlign);
+    w.hst = off; off = round_up(off + static_cast<size_t>(m * inter), kWsAlign);
+    w.hsn = off; off = round_up(off + static_cast<size_t>(m * (inter / 128)) * 8, kWsAlign);
     w.total = off;
     return w;
 }
@@ -62,7 +68,9 @@ struct FfnPtrs {
     unsigned *counters;
     float *ybuf;
     unsigned *err;
-    unsigned *gbar;
+    unsigned long long *gbar;
+    uint8_t *hst;
+    float2 *hsn;
 };
 
 FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
@@ -71,7 +79,8 @@ FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
                    reinterpret_cast<uint16_t *>(b + L.h), reinterpret_cast<int8_t *>(b + L.qh),
                    reinterpret_cast<float *>(b + L.sh), reinterpret_cast<unsigned *>(b + L.counters),
                    reinterpret_cast<float *>(b + L.ybuf), reinterpret_cast<unsigned *>(b + L.err),
-                   reinterpret_cast<unsigned *>(b + L.gbar)};
+                   reinterpret_cast<unsigned long long *>(b + L.gbar), b + L.hst,
+                   reinterpret_cast<float2 *>(b + L.hsn)};
 }
 
 tq_status check_weight(const tq_weight *w) {
@@ -80,15 +89,6 @@ tq_status check_weight(const tq_weight *w) {
     if (w->fmt != TQ_FMT_TERNARY2 && w->fmt != TQ_FMT_BINARY1) return TQ_ERR_INVALID_ARG;
     if (!aligned(w->codes, 32) || !aligned(w->scales, 2)) return TQ_ERR_ALIGNMENT;
     return TQ_OK;
-}
-
-tq_status check_smem(int fmt, int m, bool gateup, int k, int n) {
-    const size_t need = tq::gemv_smem_needed(fmt, m, gateup, k, n);
-    cudaError_t e = cudaSuccess;
-    const size_t have = tq::max_smem_optin(&e);
-    if (e != cudaSuccess) return cuda_status(e);
-    // the kernels' static shared memory (mbarriers, flags) is well under 1 KB
-    return need + 1024 <= have ? TQ_OK : TQ_ERR_UNSUPPORTED;
 }
 
 // gate [inter][hidden], up [inter][hidden], down [hidden][inter], one format
@@ -105,22 +105,11 @@ tq_status check_ffn(const tq_weight *gate, const tq_weight *up, const tq_weight 
     return TQ_OK;
 }
 
-// device limits last: every host-side check comes first
-tq_status check_ffn_smem(int fmt, int m, int hidden, int inter) {
-    tq_status st = check_smem(fmt, m, true, hidden, inter);
-    return st != TQ_OK ? st : check_smem(fmt, m, false, inter, hidden);
-}
-
 tq_status check_ws(void *ws, size_t bytes, int m, int hidden, int inter) {
     if (ws == nullptr) return TQ_ERR_INVALID_ARG;
     if (!aligned(ws, kWsAlign)) return TQ_ERR_ALIGNMENT;
     if (bytes < ffn_layout(m, hidden, inter).total) return TQ_ERR_WORKSPACE;
     return TQ_OK;
-}
-
-cudaError_t launch_gemv(const tq::GemvArgs &a, int fmt, int m, bool gateup, cudaStream_t stream) {
-    return fmt == TQ_FMT_TERNARY2 ? tq::launch_gemv_t2(a, m, gateup, stream)
-                                  : tq::launch_gemv_b1(a, m, gateup, stream);
 }
 
 cudaError_t launch_rotq(const uint16_t *x, int64_t m, int k, int8_t *q, float *s,
@@ -132,70 +121,52 @@ cudaError_t launch_rotq(const uint16_t *x, int64_t m, int k, int8_t *q, float *s
                           q, s);
 }
 
-cudaError_t launch_gateup(const tq_weight *gate, const tq_weight *up, const int8_t *qx,
-                          const float *sx, int m, uint16_t *h, int8_t *qh, float *sh,
-                          unsigned *counters, unsigned *err, cudaStream_t stream) {
-    tq::GemvArgs gu{};
-    gu.codes[0] = gate->codes;
-    gu.codes[1] = up->codes;
-    gu.scales[0] = gate->scales;
-    gu.scales[1] = up->scales;
-    gu.n = gate->n;
-    gu.k = gate->k;
-    gu.q = qx;
-    gu.s = sx;
-    gu.h = h;
-    gu.qh = qh;
-    gu.sh = sh;
-    gu.counters = counters;
-    gu.err = err;
-    return launch_gemv(gu, gate->fmt, m, true, stream);
+tq::WeightRef wref(const tq_weight *w) {
+    return tq::WeightRef{w->codes, w->scales, w->n, w->k};
 }
 
-cudaError_t launch_down(const tq_weight *down, const int8_t *qh, const float *sh, int m, float *y,
-                        unsigned *err, cudaStream_t stream) {
-    tq::GemvArgs dn{};
-    dn.codes[0] = dn.codes[1] = down->codes;
-    dn.scales[0] = dn.scales[1] = down->scales;
-    dn.n = down->n;
-    dn.k = down->k;
-    dn.q = qh;
-    dn.s = sh;
-    dn.y = y;
-    dn.err = err;
-    return launch_gemv(dn, down->fmt, m, false, stream);
+// Packed rows run in passes of at most kMaxRowsPerPass rows; the arithmetic
+// of a row does not depend on which rows share its pass.
+int pass_rows(int m, int r0) {
+    return m - r0 < tq::kMaxRowsPerPass ? m - r0 : tq::kMaxRowsPerPass;
 }
 
-bool use_fused(int fmt, int m, int hidden, int inter) {
-    if (!tq::fused_supported(fmt, m, hidden, inter)) return false;
+// device limits last: every host-side check comes first
+tq_status check_fits(const tq::Call &c) {
     cudaError_t e = cudaSuccess;
-    const size_t have = tq::max_smem_optin(&e);
-    return e == cudaSuccess && tq::fused_smem(fmt, m, hidden, inter) + 1024 <= have;
+    const bool fits = tq::call_fits(c, &e);
+    if (e != cudaSuccess) return cuda_status(e);
+    return fits ? TQ_OK : TQ_ERR_UNSUPPORTED;
 }
 
-tq::FfnFusedArgs fused_args(const FfnPtrs &P, int hidden, int inter, float eps) {
-    tq::FfnFusedArgs f{};
-    f.hidden = hidden;
-    f.inter = inter;
-    f.eps = eps;
-    f.ybuf = P.ybuf;
-    f.qx = P.qx;
-    f.sx = P.sx;
-    f.h = P.h;
-    f.qh = P.qh;
-    f.sh = P.sh;
-    f.counters = P.counters;
-    f.gbar = P.gbar;
-    f.err = P.err;
-    return f;
-}
-
-void set_layer(tq::FfnFusedArgs &f, int i, const tq_weight *g, const tq_weight *u, const tq_weight *d) {
-    const tq_weight *w[3] = {g, u, d};
-    for (int j = 0; j < 3; ++j) {
-        f.layer[i].codes[j] = w[j]->codes;
-        f.layer[i].scales[j] = w[j]->scales;
+tq::Call ffn_call(const tq_weight *gate, const tq_weight *up, const tq_weight *down, int fmt) {
+    tq::Call c{};
+    c.fmt = fmt;
+    c.m = tq::kMaxRowsPerPass;
+    if (gate != nullptr) {
+        c.do_a = 1;
+        c.wa[0] = wref(gate);
+        c.wa[1] = wref(up);
     }
+    if (down != nullptr) {
+        c.do_b = 1;
+        c.wb = wref(down);
+    }
+    return c;
+}
+
+// The workspace rows r0.. of an FFN call: every per-row array is [m][...]
+void set_ws_rows(tq::Call &c, const FfnPtrs &P, int r0, int hidden, int inter) {
+    c.qx = P.qx + static_cast<size_t>(r0) * hidden;
+    c.sx = P.sx + static_cast<size_t>(r0) * (hidden / 128);
+    c.h = P.h + static_cast<size_t>(r0) * inter;
+    c.qh = P.qh + static_cast<size_t>(r0) * inter;
+    c.sh = P.sh + static_cast<size_t>(r0) * (inter / 128);
+    c.hst = P.hst + static_cast<size_t>(r0) * inter;
+    c.hsn = P.hsn + static_cast<size_t>(r0) * (inter / 128);
+    c.hcount = P.counters;
+    c.gbar = P.gbar;
+    c.err = P.err;
 }
 
 }  // namespace
@@ -203,14 +174,6 @@ void set_layer(tq::FfnFusedArgs &f, int i, const tq_weight *g, const tq_weight *
 namespace tq {
 // lets other translation units report through tq_last_cuda_error()
 void record_cuda_error(int e) { g_last_cuda_error = e; }
-
-size_t max_smem_optin(cudaError_t *err) {
-    int dev = 0, v = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (err != nullptr) *err = e;
-    return e == cudaSuccess ? static_cast<size_t>(v) : 0;
-}
 }  // namespace tq
 
 extern "C" {
@@ -261,18 +224,20 @@ tq_status tq_gemv(const tq_weight *w, const int8_t *q, const float *s, int32_t m
     if (m < 1 || m > TQ_MAX_ROWS) return TQ_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(s, 4) || !aligned(y, 4) || !aligned(blockdots, 4))
         return TQ_ERR_ALIGNMENT;
-    st = check_smem(w->fmt, m, false, w->k, w->n);
-    if (st != TQ_OK) return st;
-    tq::GemvArgs a{};
-    a.codes[0] = a.codes[1] = w->codes;
-    a.scales[0] = a.scales[1] = w->scales;
-    a.n = w->n;
-    a.k = w->k;
-    a.q = q;
-    a.s = s;
-    a.y = y;
-    a.dots = blockdots;
-    return cuda_status(launch_gemv(a, w->fmt, m, false, reinterpret_cast<cudaStream_t>(stream)));
+    tq::Call c = ffn_call(nullptr, nullptr, w, w->fmt);
+    if ((st = check_fits(c)) != TQ_OK) return st;
+    const int nb = w->k / 128;
+    cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
+        c.m = pass_rows(m, r0);
+        c.qb = q + static_cast<size_t>(r0) * w->k;
+        c.sb = s + static_cast<size_t>(r0) * nb;
+        c.y = y + static_cast<size_t>(r0) * w->n;
+        c.dots = blockdots == nullptr ? nullptr : blockdots + static_cast<size_t>(r0) * w->n * nb;
+        e = tq::launch_call(c, str);
+    }
+    return cuda_status(e);
 }
 
 tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t *qx,
@@ -284,9 +249,20 @@ tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t
     if (m < 1 || m > TQ_MAX_ROWS) return TQ_ERR_INVALID_ARG;
     if (up->n != gate->n || up->k != gate->k || up->fmt != gate->fmt) return TQ_ERR_INVALID_ARG;
     if (!aligned(qx, 16) || !aligned(sx, 4) || !aligned(h, 2)) return TQ_ERR_ALIGNMENT;
-    if ((st = check_smem(gate->fmt, m, true, gate->k, gate->n)) != TQ_OK) return st;
-    return cuda_status(launch_gateup(gate, up, qx, sx, m, h, nullptr, nullptr, nullptr, nullptr,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+    tq::Call c = ffn_call(gate, up, nullptr, gate->fmt);
+    if ((st = check_fits(c)) != TQ_OK) return st;
+    const int hidden = gate->k, inter = gate->n;
+    cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    c.in_mode = tq::kInPlain;
+    for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
+        c.m = pass_rows(m, r0);
+        c.qa = qx + static_cast<size_t>(r0) * hidden;
+        c.sa = sx + static_cast<size_t>(r0) * (hidden / 128);
+        c.h = h + static_cast<size_t>(r0) * inter;
+        e = tq::launch_call(c, str);
+    }
+    return cuda_status(e);
 }
 
 size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter) {
@@ -320,11 +296,25 @@ tq_status tq_ffn_stage_gateup(const tq_weight *gate, const tq_weight *up, int32_
     if (m < 1 || m > TQ_MAX_ROWS) return TQ_ERR_INVALID_ARG;
     if (up->n != gate->n || up->k != gate->k || up->fmt != gate->fmt) return TQ_ERR_INVALID_ARG;
     const int hidden = gate->k, inter = gate->n;
+    if (inter % 128 != 0) return TQ_ERR_INVALID_ARG;          // h is rotated per 128-block
     if ((st = check_ws(workspace, workspace_bytes, m, hidden, inter)) != TQ_OK) return st;
-    if ((st = check_smem(gate->fmt, m, true, gate->k, gate->n)) != TQ_OK) return st;
+    tq::Call c = ffn_call(gate, up, nullptr, gate->fmt);
+    if ((st = check_fits(c)) != TQ_OK) return st;
     const FfnPtrs P = ffn_ptrs(workspace, ffn_layout(m, hidden, inter));
-    return cuda_status(launch_gateup(gate, up, P.qx, P.sx, m, P.h, P.qh, P.sh, P.counters, P.err,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    c.in_mode = tq::kInPlain;
+    c.rotate_h = 1;
+    for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
+        c.m = pass_rows(m, r0);
+        set_ws_rows(c, P, r0, hidden, inter);
+        c.qa = c.qx;
+        c.sa = c.sx;
+        c.qx = nullptr;
+        c.sx = nullptr;
+        e = tq::launch_call(c, str);
+    }
+    return cuda_status(e);
 }
 
 tq_status tq_ffn_stage_down(const tq_weight *down, int32_t m, float *y, void *workspace,
@@ -335,9 +325,20 @@ tq_status tq_ffn_stage_down(const tq_weight *down, int32_t m, float *y, void *wo
     if (!aligned(y, 4)) return TQ_ERR_ALIGNMENT;
     const int hidden = down->n, inter = down->k;
     if ((st = check_ws(workspace, workspace_bytes, m, hidden, inter)) != TQ_OK) return st;
-    if ((st = check_smem(down->fmt, m, false, down->k, down->n)) != TQ_OK) return st;
+    tq::Call c = ffn_call(nullptr, nullptr, down, down->fmt);
+    if ((st = check_fits(c)) != TQ_OK) return st;
     const FfnPtrs P = ffn_ptrs(workspace, ffn_layout(m, hidden, inter));
-    return cuda_status(launch_down(down, P.qh, P.sh, m, y, P.err, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
+        c.m = pass_rows(m, r0);
+        set_ws_rows(c, P, r0, hidden, inter);
+        c.bst = c.hst;
+        c.bsn = c.hsn;
+        c.y = y + static_cast<size_t>(r0) * hidden;
+        e = tq::launch_call(c, str);
+    }
+    return cuda_status(e);
 }
 
 tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
@@ -349,21 +350,22 @@ tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weigh
     if (!aligned(x, 16) || !aligned(y, 4)) return TQ_ERR_ALIGNMENT;
     const int hidden = gate->k, inter = gate->n;
     if ((st = check_ws(workspace, workspace_bytes, m, hidden, inter)) != TQ_OK) return st;
-    if ((st = check_ffn_smem(gate->fmt, m, hidden, inter)) != TQ_OK) return st;
+    tq::Call c = ffn_call(gate, up, down, gate->fmt);
+    if ((st = check_fits(c)) != TQ_OK) return st;
     const FfnPtrs P = ffn_ptrs(workspace, ffn_layout(m, hidden, inter));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (use_fused(gate->fmt, m, hidden, inter)) {
-        tq::FfnFusedArgs f = fused_args(P, hidden, inter, 0.0f);
-        f.num_layers = 1;
-        f.x = x;
-        f.y = y;
-        set_layer(f, 0, gate, up, down);
-        return cuda_status(tq::launch_ffn_fused(f, gate->fmt, m, s));
+    cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    c.in_mode = tq::kInRotX;
+    c.rotate_h = 1;
+    for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
+        c.m = pass_rows(m, r0);
+        set_ws_rows(c, P, r0, hidden, inter);
+        c.x = x + static_cast<size_t>(r0) * hidden;
+        c.bst = c.hst;
+        c.bsn = c.hsn;
+        c.y = y + static_cast<size_t>(r0) * hidden;
+        e = tq::launch_call(c, str);
     }
-    cudaError_t e = launch_rotq(x, m, hidden, P.qx, P.sx, s);
-    if (e == cudaSuccess)
-        e = launch_gateup(gate, up, P.qx, P.sx, m, P.h, P.qh, P.sh, P.counters, P.err, s);
-    if (e == cudaSuccess) e = launch_down(down, P.qh, P.sh, m, y, P.err, s);
     return cuda_status(e);
 }
 
@@ -381,38 +383,32 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
         if (layers[3 * l].k != hidden || layers[3 * l].n != inter) return TQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(y, 4)) return TQ_ERR_ALIGNMENT;
     if ((st = check_ws(workspace, workspace_bytes, m, hidden, inter)) != TQ_OK) return st;
-    if ((st = check_ffn_smem(layers[0].fmt, m, hidden, inter)) != TQ_OK) return st;
+    tq::Call c = ffn_call(&layers[0], &layers[1], &layers[2], layers[0].fmt);
+    if ((st = check_fits(c)) != TQ_OK) return st;
     const FfnPtrs P = ffn_ptrs(workspace, ffn_layout(m, hidden, inter));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (use_fused(layers[0].fmt, m, hidden, inter)) {
-        // chunks of up to kFusedMaxLayers layers per launch; a chunk after the
-        // first starts from the RMS-normalised output of the one before
-        cudaError_t e = cudaSuccess;
-        for (int l0 = 0; l0 < num_layers && e == cudaSuccess; l0 += tq::kFusedMaxLayers) {
-            const int cnt = num_layers - l0 < tq::kFusedMaxLayers ? num_layers - l0 : tq::kFusedMaxLayers;
-            tq::FfnFusedArgs f = fused_args(P, hidden, inter, eps);
-            f.num_layers = cnt;
-            f.input_is_y = l0 > 0;
-            f.x = x;
-            f.y_in = P.ybuf;
-            f.y = l0 + cnt == num_layers ? y : P.ybuf;
-            for (int i = 0; i < cnt; ++i)
-                set_layer(f, i, &layers[3 * (l0 + i)], &layers[3 * (l0 + i) + 1], &layers[3 * (l0 + i) + 2]);
-            e = tq::launch_ffn_fused(f, layers[0].fmt, m, s);
+    cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    c.rotate_h = 1;
+    c.eps = eps;
+    // rows are independent through the whole stack: each pass of rows runs
+    // every layer; a layer after the first starts from the RMS-normalised
+    // output of the one before (kept in ybuf, rewritten in place)
+    for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
+        c.m = pass_rows(m, r0);
+        set_ws_rows(c, P, r0, hidden, inter);
+        float *ybuf = P.ybuf + static_cast<size_t>(r0) * hidden;
+        for (int l = 0; l < num_layers && e == cudaSuccess; ++l) {
+            c.wa[0] = wref(&layers[3 * l]);
+            c.wa[1] = wref(&layers[3 * l + 1]);
+            c.wb = wref(&layers[3 * l + 2]);
+            c.in_mode = l == 0 ? tq::kInRotX : tq::kInNormY;
+            c.x = x + static_cast<size_t>(r0) * hidden;
+            c.y_in = ybuf;
+            c.bst = c.hst;
+            c.bsn = c.hsn;
+            c.y = l + 1 == num_layers ? y + static_cast<size_t>(r0) * hidden : ybuf;
+            e = tq::launch_call(c, str);
         }
-        return cuda_status(e);
-    }
-    cudaError_t e = launch_rotq(x, m, hidden, P.qx, P.sx, s);
-    for (int l = 0; l < num_layers && e == cudaSuccess; ++l) {
-        const tq_weight *L = &layers[3 * l];
-        if (l > 0)
-            e = tq::launch_pdl(tq::rmsnorm_rotq_kernel, dim3(m), dim3(tq::kNormThreads), 0, s,
-                               static_cast<const float *>(P.ybuf), hidden, eps, P.qx, P.sx,
-                               static_cast<uint16_t *>(nullptr));
-        if (e == cudaSuccess)
-            e = launch_gateup(&L[0], &L[1], P.qx, P.sx, m, P.h, P.qh, P.sh, P.counters, P.err, s);
-        if (e == cudaSuccess)
-            e = launch_down(&L[2], P.qh, P.sh, m, l + 1 == num_layers ? y : P.ybuf, P.err, s);
     }
     return cuda_status(e);
 }

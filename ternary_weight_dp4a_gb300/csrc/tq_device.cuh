@@ -12,8 +12,6 @@
 namespace tq {
 
 constexpr int kBlock = 128;        // weights per scale block / WHT size
-constexpr int kLanesPerRow = 8;    // partial sums per output (fold order)
-constexpr int kActStride = 144;    // staged activation bytes per block (128 + 16 pad)
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -36,10 +34,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
-    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
-}
-
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialisation may start while its predecessor in the stream still runs;
@@ -51,26 +45,6 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Bulk prefetch of [p, p + bytes) from global memory into L2 (p 16-byte
-// aligned, bytes a multiple of 16).  Fire and forget: nothing waits on it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Prefetch the 16-byte-aligned interior of [p, p + bytes) into L2 in chunks
-// spread over the calling lanes (never touches a byte outside the range).
-__device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes, int lane,
-                                                  int lanes) {
-    constexpr size_t kChunk = 16384;
-    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15);
-    const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes) & ~static_cast<uintptr_t>(15);
-    for (uintptr_t a = a0 + static_cast<uintptr_t>(lane) * kChunk; a < a1;
-         a += static_cast<uintptr_t>(lanes) * kChunk) {
-        const uintptr_t n = a1 - a < kChunk ? a1 - a : kChunk;
-        prefetch_l2_bulk(reinterpret_cast<const void *>(a), static_cast<uint32_t>(n));
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -146,64 +120,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// 3D tensor copy global -> shared: the box at (x, y, z) lands densely at dst
+// (x fastest); completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // Named barrier over the first `threads` threads of the CTA (id 1..15).
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// 32-/16-byte streaming loads of weight codes (each byte is read once).
-struct u32x8 { uint32_t v[8]; };
-
-__device__ __forceinline__ u32x8 ldg_stream_32B(const void *p) {
-    u32x8 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
-                   "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint4 ldg_stream_16B(const void *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
+// 16-bit read-only load (weight scales read outside the TMA path).
 __device__ __forceinline__ uint16_t ldg_u16(const uint16_t *p) {
     uint16_t r;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
     return r;
-}
-
-// ---------------------------------------------------------------------------
-// 2-bit code decode.  Codes 0, 1, 2 (values 0, +1, -1) decode to the biased
-// bytes value + 1 = 1, 2, 0 with one prmt per four codes:
-//   even codes of a word (bits 4i..4i+1) as selectors w & 0x33333333 pick
-//   byte c of kTableA = {1, 2, 0, .};
-//   odd codes (bits 4i+2..4i+3) as selectors w & 0xcccccccc have nibble
-//   4*l + 8*h: l picks byte 0 of kTableA (1) or of kTableB (2), and h sets
-//   prmt's sign-replicate mode on byte 0 of kTableA (1 -> 0x00).
-// The bias is removed exactly per block: sum((w+1)*q) - sum(q).  A word's 16
-// codes come out as the dp4a operands for weights
-//   [0 2 4 6], [8 10 12 14], [1 3 5 7], [9 11 13 15]
-// which the staged activation matches.
-// ---------------------------------------------------------------------------
-constexpr uint32_t kTableA = 0x00000201u;
-constexpr uint32_t kTableB = 0x00000002u;
-
-struct Decoded4 { uint32_t p[4]; };
-
-__device__ __forceinline__ Decoded4 decode_t2(uint32_t w) {
-    const uint32_t e = w & 0x33333333u;
-    const uint32_t o = w & 0xccccccccu;
-    Decoded4 d;
-    d.p[0] = prmt(kTableA, kTableB, e);
-    d.p[1] = prmt(kTableA, kTableB, e >> 16);
-    d.p[2] = prmt(kTableA, kTableB, o);
-    d.p[3] = prmt(kTableA, kTableB, o >> 16);
-    return d;
 }
 
 // Exact int -> float for |i| < 2^22 through the fp32 bit pattern of 2^23 + 2^22:

@@ -1,0 +1,230 @@
+// tq_kernel.cu -- shared-memory plan, tensor maps and launch of the
+// persistent GEMV / FFN kernel.
+#include <algorithm>
+#include <atomic>
+
+#include "tq.h"
+#include "tq_kernel.cuh"
+#include "tq_kernel_launch.h"
+#include "tq_tmap.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int kMaxDev = 64;
+
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+cudaError_t dev_info(DevInfo *out) {
+    static std::atomic<int> cached_sms[kMaxDev] = {};
+    static std::atomic<int> cached_smem[kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDev && cached_sms[dev].load() > 0) {
+        out->sms = cached_sms[dev].load();
+        out->smem_optin = cached_smem[dev].load();
+        return cudaSuccess;
+    }
+    if ((e = cudaDeviceGetAttribute(&out->sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&out->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    if (dev < kMaxDev) {
+        cached_smem[dev].store(out->smem_optin);
+        cached_sms[dev].store(out->sms);
+    }
+    return cudaSuccess;
+}
+
+struct Plan {
+    uint32_t off_scales, off_act, off_sn, off_part, off_tcnt;
+    size_t bytes;
+    int slots, grid;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Shared-memory plan: ring slots as many as fit (at most kMaxSlots), after
+// the activation of the larger phase, its (scale, -sum) pairs, the segment
+// sums of the largest per-CTA share of units and the tile counters.
+bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
+    const int nA = c.do_a ? c.wa[0].n : 0, kA = c.do_a ? c.wa[0].k : 0;
+    const int nB = c.do_b ? c.wb.n : 0, kB = c.do_b ? c.wb.k : 0;
+    const int tilesA = ceil_div(nA, kTileRows), tilesB = ceil_div(nB, kTileRows);
+    p->grid = (c.do_a && c.do_b) ? d.sms : std::max(1, std::min(d.sms, std::max(tilesA, tilesB)));
+    const int G = p->grid;
+    const int nbA = kA / kBlock, nbB = kB / kBlock;
+    const int nb_max = std::max(nbA, nbB);
+    const int uptA = 2 * ceil_div(nbA, kSegBlocks), uptB = ceil_div(nbB, kSegBlocks);
+    const int tpcA = ceil_div(tilesA, G), tpcB = ceil_div(tilesB, G);
+    const int units_max = std::max(tpcA * uptA, tpcB * uptB);
+    const int tiles_max = std::max(tpcA, tpcB);
+    const size_t act = static_cast<size_t>(nb_max) * kBlock * c.m;
+    const size_t sn = static_cast<size_t>(nb_max) * c.m * 8;
+    const size_t part = static_cast<size_t>(units_max) * c.m * kTileRows * 4;
+    const size_t tcnt = static_cast<size_t>(tiles_max) * 4;
+    const size_t fixed = 1024 /* alignment slack */ + align_up(act, 16) + sn + part + tcnt + 16;
+    const size_t budget = static_cast<size_t>(d.smem_optin) - 2048;   // static shared memory < 1 KB
+    if (fixed >= budget) return false;
+    const int slots = static_cast<int>(std::min<size_t>(kMaxSlots, (budget - fixed) / (kCodesSlot + kScalesSlot)));
+    if (slots < 4) return false;
+    p->slots = slots;
+    size_t off = static_cast<size_t>(slots) * kCodesSlot;
+    p->off_scales = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(slots) * kScalesSlot;
+    p->off_act = static_cast<uint32_t>(off);
+    off = align_up(off + act, 16);
+    p->off_sn = static_cast<uint32_t>(off);
+    off += sn;
+    p->off_part = static_cast<uint32_t>(off);
+    off += part;
+    p->off_tcnt = static_cast<uint32_t>(off);
+    off += tcnt;
+    p->bytes = off + 1024;
+    return true;
+}
+
+cudaError_t make_mat(MatDesc *md, const WeightRef &w, int fmt) {
+    md->codes = w.codes;
+    md->scales = w.scales;
+    md->n = w.n;
+    md->k = w.k;
+    const uint64_t row_bytes = static_cast<uint64_t>(w.k) / (fmt == TQ_FMT_TERNARY2 ? 4 : 8);
+    // 2-bit rows that are whole 128-byte planes take one 3D copy per unit
+    md->codes3d = fmt == TQ_FMT_TERNARY2 && row_bytes % 128 == 0;
+    cudaError_t e = md->codes3d
+                        ? make_codes_tmap_3d(&md->tm_codes, w.codes, row_bytes, static_cast<uint64_t>(w.n))
+                        : make_tmap_2d(&md->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, row_bytes,
+                                       static_cast<uint64_t>(w.n), row_bytes, 128, kTileRows,
+                                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    const int nb = w.k / kBlock;
+    // the scales rows are 16-byte multiples only when nb % 8 == 0; otherwise
+    // the consumers read them from global memory
+    md->scales_tma = (nb % kSegBlocks == 0) && (reinterpret_cast<uintptr_t>(w.scales) % 16 == 0);
+    if (md->scales_tma)
+        e = make_tmap_2d(&md->tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, w.scales, static_cast<uint64_t>(nb),
+                         static_cast<uint64_t>(w.n), static_cast<uint64_t>(nb) * 2, kSegBlocks, kTileRows,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    return e;
+}
+
+template <int FMT, int M>
+cudaError_t launch_t(const KArgs &a, const Plan &p, bool coop, cudaStream_t stream) {
+    auto kernel = tq_kernel<FMT, M>;
+    static std::atomic<int> configured[kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= kMaxDev || configured[dev].load() < static_cast<int>(p.bytes)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.bytes));
+        if (e != cudaSuccess) return e;
+        if (dev < kMaxDev) configured[dev].store(static_cast<int>(p.bytes));
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (coop) {
+        // the grid barrier needs every CTA resident at once
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess && coop) {
+        // a driver that refuses the two attributes together: keep the
+        // co-residency guarantee, drop the overlap with the previous launch
+        (void)cudaGetLastError();
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, a);
+    }
+    return e;
+}
+
+}  // namespace
+
+bool call_fits(const Call &c, cudaError_t *err) {
+    DevInfo d;
+    *err = dev_info(&d);
+    if (*err != cudaSuccess) return false;
+    Plan p;
+    return make_plan(c, d, &p);
+}
+
+cudaError_t launch_call(const Call &c, cudaStream_t stream) {
+    DevInfo d;
+    cudaError_t e = dev_info(&d);
+    if (e != cudaSuccess) return e;
+    Plan p;
+    if (!make_plan(c, d, &p)) return cudaErrorInvalidConfiguration;
+    KArgs a{};
+    if (c.do_a) {
+        if ((e = make_mat(&a.mat[0], c.wa[0], c.fmt)) != cudaSuccess) return e;
+        if ((e = make_mat(&a.mat[1], c.wa[1], c.fmt)) != cudaSuccess) return e;
+    }
+    if (c.do_b && (e = make_mat(&a.mat[2], c.wb, c.fmt)) != cudaSuccess) return e;
+    a.do_a = c.do_a;
+    a.do_b = c.do_b;
+    a.slots = p.slots;
+    a.off_scales = p.off_scales;
+    a.off_act = p.off_act;
+    a.off_sn = p.off_sn;
+    a.off_part = p.off_part;
+    a.off_tcnt = p.off_tcnt;
+    a.in_mode = c.in_mode;
+    a.x = c.x;
+    a.y_in = c.y_in;
+    a.eps = c.eps;
+    a.qa = c.qa;
+    a.sa = c.sa;
+    a.qx = c.qx;
+    a.sx = c.sx;
+    a.h = c.h;
+    a.rotate_h = c.rotate_h;
+    a.qh = c.qh;
+    a.sh = c.sh;
+    a.hst = c.hst;
+    a.hsn = c.hsn;
+    a.hcount = c.hcount;
+    a.bst = c.bst;
+    a.bsn = c.bsn;
+    a.qb = c.qb;
+    a.sb = c.sb;
+    a.y = c.y;
+    a.dots = c.dots;
+    a.gbar = c.gbar;
+    a.err = c.err;
+    const bool coop = c.do_a && c.do_b;
+    if (c.fmt == TQ_FMT_TERNARY2) {
+        switch (c.m) {
+            case 1: return launch_t<0, 1>(a, p, coop, stream);
+            case 2: return launch_t<0, 2>(a, p, coop, stream);
+            case 3: return launch_t<0, 3>(a, p, coop, stream);
+            default: return launch_t<0, 4>(a, p, coop, stream);
+        }
+    }
+    switch (c.m) {
+        case 1: return launch_t<1, 1>(a, p, coop, stream);
+        case 2: return launch_t<1, 2>(a, p, coop, stream);
+        case 3: return launch_t<1, 3>(a, p, coop, stream);
+        default: return launch_t<1, 4>(a, p, coop, stream);
+    }
+}
+
+}  // namespace tq

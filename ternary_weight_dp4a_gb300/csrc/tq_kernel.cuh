@@ -1,0 +1,673 @@
+// tq_kernel.cuh -- the persistent kernel behind every GEMV and FFN entry
+// point: one CTA per SM, a producer warp streaming weight tiles through a
+// shared-memory ring with tensor-map copies, fifteen consumer warps turning
+// them into exact block dots with prmt + dp4a (tq_dp4a.cuh).
+//
+// Work.  A phase multiplies m <= 4 activation rows by one or two weight
+// matrices of n rows x k.  Its unit of work is 16 weight rows x one segment
+// (8 consecutive 128-blocks) of one matrix: 4 KB of codes + 256 B of scales,
+// one ring slot.  A CTA owns whole 16-row tiles (a balanced contiguous range);
+// the units of its tiles go round-robin to its consumer warps.  Each unit
+// yields the segment sums S_j (fold order: ascending blocks from +0) of its 16
+// outputs; the warp that completes a tile's last unit folds the S_j with the
+// pairwise tree and runs the tile's epilogue.
+//
+// Phase A (gate/up): input x rotated + quantised by every CTA (or read as
+// int8), units of gate and up, epilogue h = bf16(silu(g) * u); the CTA that
+// completes the last tile of a 128-block of h rotates and quantises it.
+// Phase B (down, or a plain GEMV): input int8 rows staged from global memory,
+// epilogue y (fp32), optionally the int32 block dots.
+// A step runs A, a grid barrier, then B.  The producer never waits for the
+// consumers' phases: weights do not depend on activations, so it streams the
+// next phase's tiles (and, before griddepcontrol.wait, this launch's first
+// tiles while the previous launch drains).
+#pragma once
+
+#include <cuda.h>
+
+#include "tq_dp4a.cuh"
+#include "tq_rotq.cuh"
+
+namespace tq {
+
+constexpr int kConsumerWarps = 15;      // 14 compute warps + the epilogue warp
+constexpr int kComputeWarps = kConsumerWarps - 1;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kCodesSlot = 4096;        // 16 rows x 8 blocks of codes (2-bit: two 2 KB planes)
+constexpr int kScalesSlot = 256;        // 16 rows x 8 fp16 scales
+constexpr int kMaxSlots = 48;
+constexpr int kMaxRowsPerPass = 4;
+
+struct MatDesc {
+    CUtensorMap tm_codes;     // uint8 {row bytes, n}, box {128, 16}, 128-byte swizzle; or
+                              // (codes3d) {128, row bytes/128, n}, box {128, 2, 16}
+    CUtensorMap tm_scales;    // uint16 {k/128, n}, box {8, 16} (valid when scales_tma)
+    const uint8_t *codes;
+    const uint16_t *scales;
+    int n, k, scales_tma, codes3d;
+};
+
+enum : int { kInRotX = 0, kInNormY = 1, kInPlain = 2 };
+
+struct KArgs {
+    MatDesc mat[3];           // phase A: gate, up; phase B: mat[2]
+    int do_a, do_b;
+    int slots;                // ring slots
+    uint32_t off_scales, off_act, off_sn, off_part, off_tcnt;   // dynamic smem layout
+    // phase A input
+    int in_mode;
+    const uint16_t *x;        // bf16 [M][hidden]                 (kInRotX)
+    const float *y_in;        // fp32 [M][hidden]                 (kInNormY)
+    float eps;
+    const int8_t *qa;         // int8 [M][hidden], fp32 sa [M][hidden/128] (kInPlain)
+    const float *sa;
+    int8_t *qx;               // plain copy of the quantised input (CTA 0), may be null
+    float *sx;
+    // phase A output
+    uint16_t *h;              // bf16 [M][inter]
+    int rotate_h;
+    int8_t *qh;               // [M][inter], [M][inter/128]
+    float *sh;
+    uint8_t *hst;             // h staged for phase B: [inter/128][M][128] int8
+    float2 *hsn;              // [inter/128][M] (scale, magic - sum q as int bits)
+    unsigned *hcount;         // [inter/128]; zero on entry and on exit
+    // phase B input: staged (bst/bsn, as phase A's rotation writes them) or
+    // plain int8 qb [M][kB] + fp32 sb [M][kB/128]
+    const uint8_t *bst;
+    const float2 *bsn;
+    const int8_t *qb;
+    const float *sb;
+    float *y;                 // fp32 [M][nB]
+    int32_t *dots;            // int32 [M][nB][kB/128] or null
+    unsigned long long *gbar; // grid barrier arrivals (monotonic)
+    unsigned *err;            // bit 0: producer wait, 1: producer drain, 2: consumer wait, 4: grid barrier
+};
+
+// Tile range and unit counts of one phase for CTA c of G.
+struct PhaseGeo {
+    int n, k, nb, nseg, upt, ntiles, t0, t1, units;
+};
+
+__host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int c) {
+    PhaseGeo p{};
+    if (n <= 0) return p;
+    p.n = n;
+    p.k = k;
+    p.nb = k / kBlock;
+    p.nseg = (p.nb + kSegBlocks - 1) / kSegBlocks;
+    p.upt = nmat * p.nseg;
+    p.ntiles = (n + kTileRows - 1) / kTileRows;
+    p.t0 = static_cast<int>(static_cast<long long>(p.ntiles) * c / G);
+    p.t1 = static_cast<int>(static_cast<long long>(p.ntiles) * (c + 1) / G);
+    p.units = (p.t1 - p.t0) * p.upt;
+    return p;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier among gridDim.x co-resident CTAs, one thread per CTA:
+// a 64-bit arrival count that only grows, so a barrier is one atomic and a
+// poll until the count reaches the end of this barrier's generation.
+// Bounded: after kWaitBudgetCycles it sets err bit 4 and returns false.
+__device__ __forceinline__ bool grid_barrier(unsigned long long *gbar, unsigned *err) {
+    __threadfence();
+    const unsigned long long G = gridDim.x;
+    const unsigned long long ticket = atomicAdd(gbar, 1ull);
+    const unsigned long long target = (ticket / G + 1) * G;
+    if (ticket + 1 == target) return true;
+    const long long t0 = clock64();
+    while (ld_acquire_u64(gbar) < target) {
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            if (err != nullptr) atomicOr(err, 16u);
+            return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
+}
+
+// (scale, 0x4b400000 - sum q) of one staged block: the second word turns a
+// biased dp4a sum into the exact fp32 block dot (int_to_float_exact).
+__device__ __forceinline__ float2 block_sn(float sc, int sum) {
+    return make_float2(sc, __int_as_float(kMagic - sum));
+}
+
+// Stage one quantised block of row r (lane l holds elements l, l+32, l+64,
+// l+96 as q[0..3]) at blk = act + (b*M + r)*128; returns sum(q) over the warp.
+template <int FMT>
+__device__ __forceinline__ int stage_block_lanes(const int8_t q[4], int lane, uint8_t *blk) {
+    int sum = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        blk[staged_pos<FMT>(lane + 32 * c)] = static_cast<uint8_t>(q[c]);
+        sum += q[c];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    return sum;
+}
+
+// Stage int8 rows q [M][k] (+ fp32 s [M][k/128]) from global memory; each
+// warp loads a group of up to 4 blocks before working on any of them.
+template <int FMT, int M>
+__device__ __forceinline__ void stage_plain(const int8_t *__restrict__ q, const float *__restrict__ s,
+                                            int k, uint8_t *act, float2 *sn, int warp, int lane) {
+    const int nb = k / kBlock;
+    constexpr int kGroup = 4;
+    for (int blk0 = warp; blk0 < M * nb; blk0 += kGroup * kConsumerWarps) {
+        uint32_t w[kGroup];
+        float sc[kGroup];
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            const int blk = blk0 + u * kConsumerWarps;
+            w[u] = 0u;
+            sc[u] = 0.0f;
+            if (blk < M * nb) {
+                const int r = blk / nb, b = blk - r * nb;
+                w[u] = __ldcg(reinterpret_cast<const unsigned *>(q + static_cast<size_t>(r) * k + static_cast<size_t>(b) * kBlock) + lane);
+                sc[u] = __ldcg(s + static_cast<size_t>(r) * nb + b);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            const int blk = blk0 + u * kConsumerWarps;
+            if (blk >= M * nb) break;
+            const int r = blk / nb, b = blk - r * nb;
+            uint8_t *dst = act + static_cast<size_t>(b * M + r) * kBlock;
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int v = static_cast<int8_t>(w[u] >> (8 * i));
+                dst[staged_pos<FMT>(4 * lane + i)] = static_cast<uint8_t>(v);
+                sum += v;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) sn[b * M + r] = block_sn(sc[u], sum);
+        }
+    }
+}
+
+// Copy an activation already staged in global memory (nb blocks of 128*M
+// bytes + nb*M (scale, magic - sum) pairs) into shared memory, 16 bytes a
+// thread.
+template <int M>
+__device__ __forceinline__ void stage_copy(const uint8_t *__restrict__ st, const float2 *__restrict__ ssn,
+                                           int nb, uint8_t *act, float2 *sn, int tid) {
+    const int n16 = nb * kBlock * M / 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(st);
+    uint4 *dst = reinterpret_cast<uint4 *>(act);
+    for (int i = tid; i < n16; i += kConsumers) dst[i] = __ldcg(src + i);
+    for (int i = tid; i < nb * M; i += kConsumers) sn[i] = __ldcg(ssn + i);
+}
+
+// Rotate + quantise rows of bf16 values (in_fn(r, i) gives element i of row
+// r as a float) into the staged layout, up to kRotGroup blocks per warp at a
+// time so their shuffle chains overlap; CTA 0 also writes the plain copy.
+constexpr int kRotGroup = 3;
+
+template <int FMT, int M, typename InFn>
+__device__ __forceinline__ void stage_rotated(InFn in_fn, int k, uint8_t *act, float2 *sn, int warp,
+                                              int lane, int8_t *q_out, float *s_out, int r_only = -1) {
+    const int nb = k / kBlock;
+    const int rows = r_only >= 0 ? 1 : M;
+    for (int blk0 = warp; blk0 < rows * nb; blk0 += kRotGroup * kConsumerWarps) {
+        float v[kRotGroup][4];
+#pragma unroll
+        for (int u = 0; u < kRotGroup; ++u) {
+            const int blk = blk0 + u * kConsumerWarps;
+            const int r = r_only >= 0 ? r_only : blk / nb;
+            const int b = r_only >= 0 ? blk : blk - r * nb;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[u][c] = blk < rows * nb ? in_fn(r, b * kBlock + lane + 32 * c) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kRotGroup; ++u) wht128_warp(v[u], lane);
+#pragma unroll
+        for (int u = 0; u < kRotGroup; ++u) {
+            const int blk = blk0 + u * kConsumerWarps;
+            if (blk >= rows * nb) break;
+            const int r = r_only >= 0 ? r_only : blk / nb;
+            const int b = r_only >= 0 ? blk : blk - r * nb;
+            int8_t q[4];
+            const float sc = quant_block_warp(v[u], q);
+            const int sum = stage_block_lanes<FMT>(q, lane, act + static_cast<size_t>(b * M + r) * kBlock);
+            if (lane == 0) sn[b * M + r] = block_sn(sc, sum);
+            if (q_out != nullptr) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) q_out[static_cast<size_t>(r) * k + b * kBlock + lane + 32 * c] = q[c];
+                if (lane == 0) s_out[static_cast<size_t>(r) * nb + b] = sc;
+            }
+        }
+    }
+}
+
+// Pairwise tree over V[0..cnt) (stride `stride` floats), in place: each level
+// adds (0,1), (2,3), ... and passes an odd last node up.
+__device__ __forceinline__ float fold_tree(float *V, int cnt, int stride) {
+    while (cnt > 1) {
+        int nxt = 0;
+        for (int i = 0; i + 1 < cnt; i += 2, ++nxt)
+            V[nxt * stride] = __fadd_rn(V[i * stride], V[(i + 1) * stride]);
+        if (cnt & 1) {
+            V[nxt * stride] = V[(cnt - 1) * stride];
+            ++nxt;
+        }
+        cnt = nxt;
+    }
+    return V[0];
+}
+
+// One 128-block of a unit: decode, four MMAs, exact block dot, and the
+// fold step t_b into the segment sums of weight rows g and g+8.
+// One unit: 16 weight rows x the segment's blocks.  Lane l = 16h + r works
+// on row r, half h of every block (2-bit: words 4h..4h+3, 64 weights; 1-bit:
+// words 2h, 2h+1); the halves' dp4a sums meet in one shuffle and lane r
+// (h = 0) folds t_b = (float)d * (ws * sa) into the segment sums acc[mm]
+// in ascending block order.
+template <int FMT, int M, bool DOTS>
+__device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
+                                          int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
+                                          int32_t *dots, int row, int n, int nb) {
+    const int r = lane & 15, h = lane >> 4;
+    const int sw = r & 7;                                   // 128-byte swizzle of the row
+#pragma unroll
+    for (int bl = 0; bl < kSegBlocks; ++bl) {
+        if (bl >= bcount) break;
+        const int b = b0 + bl;
+        int dot[M];
+#pragma unroll
+        for (int mm = 0; mm < M; ++mm) dot[mm] = 0;
+        const uint8_t *ab = act + static_cast<size_t>(b) * M * kBlock + h * 64;
+        if constexpr (FMT == 0) {
+            // 128-byte line of (row r, plane bl/4): 3D copies lay rows out
+            // [row][plane], 2D copies [plane][row]; the swizzle XORs the
+            // 16-byte chunk with the line index mod 8
+            const int line = codes3d ? 2 * r + (bl >> 2) : (bl >> 2) * kTileRows + r;
+            const uint4 cw = *reinterpret_cast<const uint4 *>(cs + line * 128 +
+                                                              ((((bl & 3) * 2 + h) ^ (line & 7)) * 16));
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t p0, p1, p2, p3;
+                decode_t2(words[i], p0, p1, p2, p3);
+#pragma unroll
+                for (int mm = 0; mm < M; ++mm) {
+                    const uint4 av = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 16);
+                    dot[mm] = __dp4a(static_cast<int>(p0), static_cast<int>(av.x), dot[mm]);
+                    dot[mm] = __dp4a(static_cast<int>(p1), static_cast<int>(av.y), dot[mm]);
+                    dot[mm] = __dp4a(static_cast<int>(p2), static_cast<int>(av.z), dot[mm]);
+                    dot[mm] = __dp4a(static_cast<int>(p3), static_cast<int>(av.w), dot[mm]);
+                }
+            }
+        } else {
+            const uint2 cw = *reinterpret_cast<const uint2 *>(cs + r * 128 + ((bl ^ sw) * 16) + h * 8);
+            const uint32_t words[2] = {cw.x, cw.y};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+#pragma unroll
+                for (int mm = 0; mm < M; ++mm) {
+                    const uint4 a0 = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 32);
+                    const uint4 a1 = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 32 + 16);
+                    const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                    for (int sb = 0; sb < 8; ++sb)
+                        dot[mm] = __dp4a(static_cast<int>((words[i] >> sb) & 0x01010101u), static_cast<int>(av[sb]), dot[mm]);
+                }
+            }
+        }
+        const uint32_t wsw = wsr[bl >> 1];
+        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
+#pragma unroll
+        for (int mm = 0; mm < M; ++mm) {
+            int d = dot[mm] + __shfl_xor_sync(0xffffffffu, dot[mm], 16);
+            if (FMT == 1) d *= 2;
+            const float2 sv = sn[b * M + mm];                // (activation scale, magic - sum q)
+            const float v = int_to_float_exact(d, __float_as_int(sv.y));
+            acc[mm] = __fadd_rn(acc[mm], __fmul_rn(v, __fmul_rn(ws, sv.x)));
+            if constexpr (DOTS)
+                if (h == 0 && row < n) dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
+        }
+    }
+}
+
+template <int FMT, int M>
+__global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__ KArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxSlots];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxSlots];
+    __shared__ float s_warp[8];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int S = a.slots;
+    uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *codes_ring = base;
+    const uint16_t *scales_ring = reinterpret_cast<const uint16_t *>(base + a.off_scales);
+    uint8_t *act = base + a.off_act;
+    float2 *sn = reinterpret_cast<float2 *>(base + a.off_sn);
+    float *part = reinterpret_cast<float *>(base + a.off_part);
+    int *tcnt = reinterpret_cast<int *>(base + a.off_tcnt);
+
+    const PhaseGeo ga = a.do_a ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta) : PhaseGeo{};
+    const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta) : PhaseGeo{};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        // units in order: phase A (tile, gate/up, segment), then phase B
+        // (tile, segment).  Lanes 0..kProducerLanes-1 each issue every
+        // kProducerLanes-th unit, so several units are in the issue pipe at
+        // once; (lt, ru) and (slot, round) = divmod(k, S) advance incrementally.
+        constexpr int kProducerLanes = 4;
+        const int total = ga.units + gb.units;
+        if (lane < kProducerLanes) {
+            bool ok = true;
+            int k = lane;
+            bool in_a = k < ga.units;
+            int lt, ru;
+            {
+                const int i0 = in_a ? k : k - ga.units;
+                const int upt = in_a ? ga.upt : max(gb.upt, 1);
+                lt = i0 / upt;
+                ru = i0 - lt * upt;
+            }
+            int slot = k % S, round = k / S;
+            for (; k < total && ok; k += kProducerLanes) {
+                if (in_a && k >= ga.units) {
+                    in_a = false;
+                    const int i0 = k - ga.units;
+                    lt = i0 / gb.upt;
+                    ru = i0 - lt * gb.upt;
+                }
+                const PhaseGeo &P = in_a ? ga : gb;
+                const int mi = in_a ? (ru >= P.nseg ? 1 : 0) : 2;
+                const int seg = in_a && ru >= P.nseg ? ru - P.nseg : ru;
+                const int tile = P.t0 + lt;
+                const MatDesc &md = a.mat[mi];
+                if (round > 0 && !(ok = mbar_wait(smem_u32(&empty_bar[slot]), (round - 1) & 1))) break;
+                const uint32_t fb = smem_u32(&full_bar[slot]);
+                const uint32_t dst = smem_u32(codes_ring + static_cast<size_t>(slot) * kCodesSlot);
+                const bool sct = md.scales_tma != 0;
+                if (FMT == 0 && md.codes3d) {
+                    mbar_arrive_expect_tx(fb, 4096u + (sct ? kScalesSlot : 0u));
+                    tma_load_3d(dst, &md.tm_codes, 0, seg * 2, tile * kTileRows, fb);
+                } else {
+                    const int planes = FMT == 0 ? (seg * kSegBlocks + 4 < P.nb ? 2 : 1) : 1;
+                    mbar_arrive_expect_tx(fb, planes * 2048u + (sct ? kScalesSlot : 0u));
+                    const int x0 = FMT == 0 ? seg * kSegBlocks * 32 : seg * kSegBlocks * 16;
+                    tma_load_2d(dst, &md.tm_codes, x0, tile * kTileRows, fb);
+                    if (planes == 2) tma_load_2d(dst + 2048, &md.tm_codes, x0 + 128, tile * kTileRows, fb);
+                }
+                if (sct)
+                    tma_load_2d(smem_u32(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2)), &md.tm_scales,
+                                seg * kSegBlocks, tile * kTileRows, fb);
+                ru += kProducerLanes;
+                while (ru >= P.upt) {
+                    ru -= P.upt;
+                    ++lt;
+                }
+                slot += kProducerLanes;
+                if (slot >= S) {
+                    slot -= S;
+                    ++round;
+                }
+            }
+            if (!ok && a.err != nullptr) atomicOr(a.err, 1u);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            // no copy may still be landing in shared memory when the CTA exits
+            const int k0 = total > S ? total - S : 0;
+            int slot = k0 % S, round = k0 / S;
+            for (int k = k0; k < total; ++k) {
+                if (!mbar_wait(smem_u32(&full_bar[slot]), round & 1) && a.err != nullptr) atomicOr(a.err, 2u);
+                if (++slot == S) {
+                    slot = 0;
+                    ++round;
+                }
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int tid = threadIdx.x;             // 0 .. kConsumers-1
+    bool ok = true;
+    pdl_wait();
+
+    for (int ph = 0; ph < 2; ++ph) {
+        const bool is_a = ph == 0;
+        if (is_a ? !a.do_a : !a.do_b) continue;
+        const PhaseGeo &P = is_a ? ga : gb;
+        const int kbase = is_a ? 0 : ga.units;
+
+        // ---- stage this phase's activation
+        if (is_a) {
+            if (a.in_mode == kInRotX) {
+                const uint16_t *x = a.x;
+                const int hidden = P.k;
+                stage_rotated<FMT, M>([&](int r, int i) { return bf16_bits_to_f32(x[static_cast<size_t>(r) * hidden + i]); },
+                                      P.k, act, sn, warp, lane, cta == 0 ? a.qx : nullptr, a.sx);
+            } else if (a.in_mode == kInNormY) {
+                const int hidden = P.k;
+                for (int r = 0; r < M; ++r) {
+                    // 1/rms: 256 partial sums (thread i adds y[i], y[i+256], ...),
+                    // each warp's 32 combined at distance 1, 2, ..., 16, then
+                    // ((w0+w1)+(w2+w3)) + ((w4+w5)+(w6+w7))
+                    const float *yr = a.y_in + static_cast<size_t>(r) * hidden;
+                    float acc = 0.0f;
+                    if (tid < 256)
+                        for (int i = tid; i < hidden; i += 256) {
+                            const float v = __ldcg(yr + i);
+                            acc = __fadd_rn(acc, __fmul_rn(v, v));
+                        }
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+                    if (lane == 0 && warp < 8) s_warp[warp] = acc;
+                    named_barrier(1, kConsumers);
+                    const float w01 = __fadd_rn(s_warp[0], s_warp[1]), w23 = __fadd_rn(s_warp[2], s_warp[3]);
+                    const float w45 = __fadd_rn(s_warp[4], s_warp[5]), w67 = __fadd_rn(s_warp[6], s_warp[7]);
+                    const float ss = __fadd_rn(__fadd_rn(w01, w23), __fadd_rn(w45, w67));
+                    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hidden)), a.eps)));
+                    named_barrier(1, kConsumers);
+                    stage_rotated<FMT, M>([&](int, int i) {
+                        return bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__ldcg(yr + i), inv)));
+                    }, hidden, act, sn, warp, lane, cta == 0 ? a.qx : nullptr, a.sx, r);
+                }
+            } else {
+                stage_plain<FMT, M>(a.qa, a.sa, P.k, act, sn, warp, lane);
+            }
+        } else if (a.bst != nullptr) {
+            stage_copy<M>(a.bst, a.bsn, P.nb, act, sn, tid);
+        } else {
+            stage_plain<FMT, M>(a.qb, a.sb, P.k, act, sn, warp, lane);
+        }
+        for (int i = tid; i < P.t1 - P.t0; i += kConsumers) tcnt[i] = 0;
+        named_barrier(1, kConsumers);
+
+        // ---- units of this phase: CTA-local index k, compute warp k % 14;
+        // (lt, ru) = divmod(k - kbase, upt) and (slot, round) = divmod(k, S)
+        // advance incrementally.  A compute warp never waits on anything but
+        // its data: tile epilogues run on the epilogue warp.
+        if (warp < kComputeWarps) {
+        int k = kbase + ((warp - kbase) % kComputeWarps + kComputeWarps) % kComputeWarps;
+        int lt = (k - kbase) / max(P.upt, 1), ru = (k - kbase) - lt * P.upt;
+        int slot = k % S, round = k / S;
+        for (; k < kbase + P.units; k += kComputeWarps) {
+            if (ok && !mbar_wait(smem_u32(&full_bar[slot]), round & 1)) ok = false;
+            if (!ok) break;
+            const int i = k - kbase;
+            const int mi = is_a ? (ru >= P.nseg ? 1 : 0) : 2;
+            const int seg = is_a && ru >= P.nseg ? ru - P.nseg : ru;
+            const int tile = P.t0 + lt;
+            const MatDesc &md = a.mat[mi];
+            const uint8_t *cs = codes_ring + static_cast<size_t>(slot) * kCodesSlot;
+            const int bcount = min(kSegBlocks, P.nb - seg * kSegBlocks);
+
+            // weight scales of row r of the tile for the segment's blocks
+            const int rr16 = lane & 15;
+            const int row = tile * kTileRows + rr16;
+            uint32_t wsr[4];
+            if (md.scales_tma) {
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2) + rr16 * 8);
+                wsr[0] = u0.x; wsr[1] = u0.y; wsr[2] = u0.z; wsr[3] = u0.w;
+            } else {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t lo = 0, hi = 0;
+                    const int bb = seg * kSegBlocks + 2 * w;
+                    if (row < P.n && 2 * w < bcount) lo = ldg_u16(md.scales + static_cast<size_t>(row) * P.nb + bb);
+                    if (row < P.n && 2 * w + 1 < bcount) hi = ldg_u16(md.scales + static_cast<size_t>(row) * P.nb + bb + 1);
+                    wsr[w] = lo | (hi << 16);
+                }
+            }
+
+            float acc[M];
+#pragma unroll
+            for (int mm = 0; mm < M; ++mm) acc[mm] = 0.0f;
+            if (!is_a && a.dots != nullptr)
+                unit_dp4a<FMT, M, true>(cs, md.codes3d != 0, act, sn, seg * kSegBlocks, bcount, wsr, lane, acc, a.dots, row, P.n, P.nb);
+            else
+                unit_dp4a<FMT, M, false>(cs, md.codes3d != 0, act, sn, seg * kSegBlocks, bcount, wsr, lane, acc, nullptr, row, P.n, P.nb);
+            // the slot's codes and scales are all in registers: hand it back
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+            // advance to this warp's next unit
+            const int lt_done = lt;
+            ru += kComputeWarps;
+            while (ru >= P.upt) {
+                ru -= P.upt;
+                ++lt;
+            }
+            slot += kComputeWarps;
+            while (slot >= S) {
+                slot -= S;
+                ++round;
+            }
+
+            // segment sums of this unit -> shared memory; count the tile
+            float *pu = part + static_cast<size_t>(i) * M * kTileRows;
+            if (lane < kTileRows) {
+#pragma unroll
+                for (int mm = 0; mm < M; ++mm) pu[mm * kTileRows + lane] = acc[mm];
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                atomicAdd(&tcnt[lt_done], 1);
+            }
+        }
+        } else {
+        // ---- epilogue warp: tiles in order, each once all its units are in
+        const volatile int *vt = tcnt;
+        for (int lt_done = 0; lt_done < P.t1 - P.t0; ++lt_done) {
+            const long long w0 = clock64();
+            while (vt[lt_done] < P.upt) {
+                if (clock64() - w0 > kWaitBudgetCycles) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
+            }
+            if (!ok) break;
+            __threadfence_block();
+            const int tile = P.t0 + lt_done;
+            const int rr16 = lane & 15;
+            const int row = tile * kTileRows + rr16;
+
+            // ---- tile epilogue: fold the segment sums with the pairwise tree
+            const int r = lane >> 4;            // activation rows r, r + 2, ... of the tile's 16 outputs
+            float *pt = part + static_cast<size_t>(lt_done) * P.upt * M * kTileRows + r * kTileRows + rr16;
+            if (is_a) {
+                for (int ra = r; ra < M; ra += 2) {
+                    float *pr = pt + (ra - r) * kTileRows;
+                    const float gv = fold_tree(pr, P.nseg, M * kTileRows);
+                    const float uv = fold_tree(pr + static_cast<size_t>(P.nseg) * M * kTileRows, P.nseg, M * kTileRows);
+                    if (row < P.n)
+                        a.h[static_cast<size_t>(ra) * P.n + row] = f32_to_bf16_bits(__fmul_rn(tq_silu(gv), uv));
+                }
+                if (a.rotate_h) {
+                    // the CTA completing the last tile of a 128-block of h rotates it
+                    __syncwarp();
+                    const int hb = tile * kTileRows / kBlock;
+                    const unsigned add = static_cast<unsigned>(min(kTileRows, P.n - tile * kTileRows));
+                    int hlast = 0;
+                    if (lane == 0) {
+                        __threadfence();
+                        hlast = atomicAdd(&a.hcount[hb], add) + add == static_cast<unsigned>(kBlock);
+                    }
+                    hlast = __shfl_sync(0xffffffffu, hlast, 0);
+                    if (hlast) {
+                        __threadfence();
+                        const int nbh = P.n / kBlock;
+                        float v[M][4];
+#pragma unroll
+                        for (int rr = 0; rr < M; ++rr)
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc)
+                                v[rr][cc] = bf16_bits_to_f32(__ldcg(a.h + static_cast<size_t>(rr) * P.n + hb * kBlock + lane + 32 * cc));
+#pragma unroll
+                        for (int rr = 0; rr < M; ++rr) wht128_warp(v[rr], lane);
+#pragma unroll
+                        for (int rr = 0; rr < M; ++rr) {
+                            int8_t q[4];
+                            const float sc = quant_block_warp(v[rr], q);
+                            int sum = 0;
+                            uint8_t *hst = a.hst + static_cast<size_t>(hb * M + rr) * kBlock;
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc) {
+                                const int e = lane + 32 * cc;
+                                a.qh[static_cast<size_t>(rr) * P.n + hb * kBlock + e] = q[cc];
+                                hst[staged_pos<FMT>(e)] = static_cast<uint8_t>(q[cc]);
+                                sum += q[cc];
+                            }
+#pragma unroll
+                            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                            if (lane == 0) {
+                                a.sh[static_cast<size_t>(rr) * nbh + hb] = sc;
+                                a.hsn[hb * M + rr] = block_sn(sc, sum);
+                            }
+                        }
+                        if (lane == 0) a.hcount[hb] = 0u;
+                    }
+                }
+            } else {
+                for (int ra = r; ra < M; ra += 2) {
+                    const float yv = fold_tree(pt + (ra - r) * kTileRows, P.nseg, M * kTileRows);
+                    if (row < P.n) a.y[static_cast<size_t>(ra) * P.n + row] = yv;
+                }
+            }
+        }
+        }
+        named_barrier(1, kConsumers);
+        if (is_a && a.do_b) {
+            // every CTA's h blocks are rotated before phase B reads them
+            if (tid == 0 && !grid_barrier(a.gbar, a.err)) ok = false;
+            named_barrier(1, kConsumers);
+        }
+    }
+    if (!ok && lane == 0 && a.err != nullptr) atomicOr(a.err, 4u);
+}
+
+}  // namespace tq

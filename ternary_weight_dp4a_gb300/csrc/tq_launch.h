@@ -1,16 +1,17 @@
-// tq_launch.h -- host-side launch helpers shared by the libtq translation units.
+// tq_launch.h -- host-side launch helper shared by the libtq translation units.
 #pragma once
 
 #include <cuda_runtime.h>
 
-#include "tq_gemv.cuh"
+#include <utility>
 
 namespace tq {
 
 // Launch `kernel` with programmatic stream serialisation: it may start while
 // the previous work in the stream drains, and synchronises inside through
 // pdl_wait().  Every libtq kernel reads nothing produced by earlier stream
-// work before that wait.
+// work before that wait (weights excepted: nothing in a stream of libtq calls
+// writes them).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args &&...args) {
@@ -26,16 +27,5 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
-
-// Launch the GEMV (gateup = false) or the fused gate/up + SiLU*up kernel for
-// format fmt and m packed rows.  Arguments are already validated.
-cudaError_t launch_gemv_t2(const GemvArgs &a, int m, bool gateup, cudaStream_t stream);
-cudaError_t launch_gemv_b1(const GemvArgs &a, int m, bool gateup, cudaStream_t stream);
-
-// Largest dynamic shared memory a CTA may use on the current device.
-size_t max_smem_optin(cudaError_t *err = nullptr);
-
-// Dynamic shared memory the GEMV kernel for (fmt, m, gateup) needs at (k, n).
-size_t gemv_smem_needed(int fmt, int m, bool gateup, int k, int n);
 
 }  // namespace tq

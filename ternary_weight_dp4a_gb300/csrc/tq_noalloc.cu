@@ -20,7 +20,7 @@ constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // The FFN workspace at the largest sizes, laid out as tq_ffn_step lays it out
 // (every section 256-byte aligned): qx, sx, h, qh, sh, counters, ybuf, err,
-// grid-barrier words.
+// grid-barrier count, staged h and its (scale, -sum) pairs.
 constexpr size_t kStaticBytes =
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden) +
     align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxHidden / 128) * 4) +
@@ -28,7 +28,9 @@ constexpr size_t kStaticBytes =
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
     align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 4) +
     align256(static_cast<size_t>(kStaticMaxInter / 128) * 4) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden * 4) + align256(4) + align256(8);
+    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden * 4) + align256(4) + align256(8) +
+    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
+    align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 8);
 
 // One copy per GPU that loads the library, held until the process exits.
 // Device code could name it directly; host code must use the address from
