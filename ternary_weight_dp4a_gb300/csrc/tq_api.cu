@@ -33,12 +33,13 @@ constexpr size_t kWsAlign = 256;
 //   qx int8 [m][hidden] | sx f32 [m][hidden/128] | h bf16 [m][inter] |
 //   qh int8 [m][inter]  | sh f32 [m][inter/128]  | counters u32 [inter/128] |
 //   ybuf f32 [m][hidden] | err u32 (nonzero: a kernel's bounded wait ran out) |
-//   gbar u64 (grid-barrier arrivals of the step kernel; only ever grows) |
+//   sync u32 [2 + inter/1024] (the step kernel's count of CTAs done and, per
+//   1024-wide segment of h, its rotated 128-blocks; zero between calls) |
 //   hst i8 [m*inter] (h quantised again, staged as the down phase reads it:
 //   per pass of rows r0.., [inter/128][rows][128] permuted) |
 //   hsn (f32 scale, i32 0x4b400000 - sum q) [m][inter/128]
 struct FfnWorkspace {
-    size_t qx, sx, h, qh, sh, counters, ybuf, err, gbar, hst, hsn, total;
+    size_t qx, sx, h, qh, sh, counters, ybuf, err, sync, hst, hsn, total;
 };
 
 FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
@@ -52,7 +53,7 @@ FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
     w.counters = off; off = round_up(off + static_cast<size_t>(inter / 128) * 4, kWsAlign);
     w.ybuf = off; off = round_up(off + static_cast<size_t>(m * hidden) * 4, kWsAlign);
     w.err = off; off = round_up(off + 4, kWsAlign);
-    w.gbar = off; off = round_up(off + 8, kWsAlign);
+    w.sync = off; off = round_up(off + static_cast<size_t>(2 + (inter + 1023) / 1024) * 4, kWsAlign);
     w.hst = off; off = round_up(off + static_cast<size_t>(m * inter), kWsAlign);
     w.hsn = off; off = round_up(off + static_cast<size_t>(m * (inter / 128)) * 8, kWsAlign);
     w.total = off;
@@ -68,7 +69,8 @@ struct FfnPtrs {
     unsigned *counters;
     float *ybuf;
     unsigned *err;
-    unsigned long long *gbar;
+    unsigned *done;
+    unsigned *segready;
     uint8_t *hst;
     float2 *hsn;
 };
@@ -79,7 +81,7 @@ FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
                    reinterpret_cast<uint16_t *>(b + L.h), reinterpret_cast<int8_t *>(b + L.qh),
                    reinterpret_cast<float *>(b + L.sh), reinterpret_cast<unsigned *>(b + L.counters),
                    reinterpret_cast<float *>(b + L.ybuf), reinterpret_cast<unsigned *>(b + L.err),
-                   reinterpret_cast<unsigned long long *>(b + L.gbar), b + L.hst,
+                   reinterpret_cast<unsigned *>(b + L.sync), reinterpret_cast<unsigned *>(b + L.sync) + 1, b + L.hst,
                    reinterpret_cast<float2 *>(b + L.hsn)};
 }
 
@@ -165,7 +167,8 @@ void set_ws_rows(tq::Call &c, const FfnPtrs &P, int r0, int hidden, int inter) {
     c.hst = P.hst + static_cast<size_t>(r0) * inter;
     c.hsn = P.hsn + static_cast<size_t>(r0) * (inter / 128);
     c.hcount = P.counters;
-    c.gbar = P.gbar;
+    c.done = P.done;
+    c.segready = P.segready;
     c.err = P.err;
 }
 

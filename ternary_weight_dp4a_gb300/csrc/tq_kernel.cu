@@ -41,9 +41,9 @@ cudaError_t dev_info(DevInfo *out) {
 }
 
 struct Plan {
-    uint32_t off_scales, off_act, off_sn, off_part, off_tcnt;
+    uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt;
     size_t bytes;
-    int slots, grid;
+    int slots, grid, tiles_max, nseg_max;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -51,25 +51,32 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Shared-memory plan: ring slots as many as fit (at most kMaxSlots), after
-// the activation of the larger phase, its (scale, -sum) pairs, the segment
-// sums of the largest per-CTA share of units and the tile counters.
+// both phases' activations and (scale, magic - sum) pairs, the segment sums
+// of the largest per-CTA share of units of each phase and the counters.
 bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     const int nA = c.do_a ? c.wa[0].n : 0, kA = c.do_a ? c.wa[0].k : 0;
     const int nB = c.do_b ? c.wb.n : 0, kB = c.do_b ? c.wb.k : 0;
     const int tilesA = ceil_div(nA, kTileRows), tilesB = ceil_div(nB, kTileRows);
+    // a launch running both phases needs every CTA resident (phase B waits on
+    // blocks of h other CTAs rotate): one CTA per SM
     p->grid = (c.do_a && c.do_b) ? d.sms : std::max(1, std::min(d.sms, std::max(tilesA, tilesB)));
     const int G = p->grid;
     const int nbA = kA / kBlock, nbB = kB / kBlock;
-    const int nb_max = std::max(nbA, nbB);
     const int uptA = 2 * ceil_div(nbA, kSegBlocks), uptB = ceil_div(nbB, kSegBlocks);
-    const int tpcA = ceil_div(tilesA, G), tpcB = ceil_div(tilesB, G);
-    const int units_max = std::max(tpcA * uptA, tpcB * uptB);
-    const int tiles_max = std::max(tpcA, tpcB);
-    const size_t act = static_cast<size_t>(nb_max) * kBlock * c.m;
-    const size_t sn = static_cast<size_t>(nb_max) * c.m * 8;
-    const size_t part = static_cast<size_t>(units_max) * c.m * kTileRows * 4;
-    const size_t tcnt = static_cast<size_t>(tiles_max) * 4;
-    const size_t fixed = 1024 /* alignment slack */ + align_up(act, 16) + sn + part + tcnt + 16;
+    const int tpcA = c.do_a ? phase_tiles_max(nA, G) : 0, tpcB = c.do_b ? phase_tiles_max(nB, G) : 0;
+    // the epilogue warp tracks this CTA's phase-A tiles in a 32-bit mask
+    if (c.do_a && c.rotate_h && tpcA > 32) return false;
+    p->tiles_max = std::max(1, std::max(tpcA, tpcB));
+    p->nseg_max = std::max(1, uptB);
+    const size_t actA = static_cast<size_t>(nbA) * kBlock * c.m, snA = static_cast<size_t>(nbA) * c.m * 8;
+    const size_t actB = static_cast<size_t>(nbB) * kBlock * c.m, snB = static_cast<size_t>(nbB) * c.m * 8;
+    const size_t part = static_cast<size_t>(tpcA * uptA + tpcB * uptB) * c.m * kTileRows * 4;
+    const size_t ints = static_cast<size_t>(3 * p->tiles_max + p->nseg_max) * 4;
+    // every region starts on a 128-byte boundary (the activations are read
+    // and written 16 bytes at a time)
+    constexpr size_t kAlign = 128;
+    const size_t fixed = 1024 /* alignment slack */ + align_up(actA, kAlign) + align_up(snA, kAlign) + align_up(actB, kAlign) +
+                         align_up(snB, kAlign) + align_up(part, kAlign) + align_up(ints, kAlign);
     const size_t budget = static_cast<size_t>(d.smem_optin) - 2048;   // static shared memory < 1 KB
     if (fixed >= budget) return false;
     const int slots = static_cast<int>(std::min<size_t>(kMaxSlots, (budget - fixed) / (kCodesSlot + kScalesSlot)));
@@ -79,13 +86,17 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     p->off_scales = static_cast<uint32_t>(off);
     off += static_cast<size_t>(slots) * kScalesSlot;
     p->off_act = static_cast<uint32_t>(off);
-    off = align_up(off + act, 16);
+    off = align_up(off + actA, kAlign);
     p->off_sn = static_cast<uint32_t>(off);
-    off += sn;
+    off = align_up(off + snA, kAlign);
+    p->off_acth = static_cast<uint32_t>(off);
+    off = align_up(off + actB, kAlign);
+    p->off_snh = static_cast<uint32_t>(off);
+    off = align_up(off + snB, kAlign);
     p->off_part = static_cast<uint32_t>(off);
-    off += part;
+    off = align_up(off + part, kAlign);
     p->off_tcnt = static_cast<uint32_t>(off);
-    off += tcnt;
+    off = align_up(off + ints, kAlign);
     p->bytes = off + 1024;
     return true;
 }
@@ -185,8 +196,12 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.off_scales = p.off_scales;
     a.off_act = p.off_act;
     a.off_sn = p.off_sn;
+    a.off_acth = p.off_acth;
+    a.off_snh = p.off_snh;
     a.off_part = p.off_part;
     a.off_tcnt = p.off_tcnt;
+    a.tiles_max = p.tiles_max;
+    a.nseg_max = p.nseg_max;
     a.in_mode = c.in_mode;
     a.x = c.x;
     a.y_in = c.y_in;
@@ -208,9 +223,10 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.sb = c.sb;
     a.y = c.y;
     a.dots = c.dots;
-    a.gbar = c.gbar;
+    a.segready = c.segready;
+    a.done = c.done;
     a.err = c.err;
-    const bool coop = c.do_a && c.do_b;
+    const bool coop = c.do_a && c.do_b;     // phase B waits on other CTAs' rotations
     if (c.fmt == TQ_FMT_TERNARY2) {
         switch (c.m) {
             case 1: return launch_t<0, 1>(a, p, coop, stream);

@@ -6,8 +6,8 @@
 // Work.  A phase multiplies m <= 4 activation rows by one or two weight
 // matrices of n rows x k.  Its unit of work is 16 weight rows x one segment
 // (8 consecutive 128-blocks) of one matrix: 4 KB of codes + 256 B of scales,
-// one ring slot.  A CTA owns whole 16-row tiles (a balanced contiguous range);
-// the units of its tiles go round-robin to its consumer warps.  Each unit
+// one ring slot.  A CTA owns whole 16-row tiles (dealt out strided, see
+// phase_geo); the units of its tiles go round-robin to its compute warps.  Each unit
 // yields the segment sums S_j (fold order: ascending blocks from +0) of its 16
 // outputs; the warp that completes a tile's last unit folds the S_j with the
 // pairwise tree and runs the tile's epilogue.
@@ -17,10 +17,12 @@
 // completes the last tile of a 128-block of h rotates and quantises it.
 // Phase B (down, or a plain GEMV): input int8 rows staged from global memory,
 // epilogue y (fp32), optionally the int32 block dots.
-// A step runs A, a grid barrier, then B.  The producer never waits for the
-// consumers' phases: weights do not depend on activations, so it streams the
-// next phase's tiles (and, before griddepcontrol.wait, this launch's first
-// tiles while the previous launch drains).
+// A step runs A and B in one launch without a grid barrier: a phase-B unit
+// waits only until the 8 blocks of h its segment reads are rotated.  The
+// producer never waits for the consumers' phases: weights do not depend on
+// activations, so it streams the next phase's tiles (and, before
+// griddepcontrol.wait, this launch's first tiles while the previous launch
+// drains).
 #pragma once
 
 #include <cuda.h>
@@ -38,6 +40,7 @@ constexpr int kCodesSlot = 4096;        // 16 rows x 8 blocks of codes (2-bit: t
 constexpr int kScalesSlot = 256;        // 16 rows x 8 fp16 scales
 constexpr int kMaxSlots = 48;
 constexpr int kMaxRowsPerPass = 4;
+constexpr int kTilesPerHBlock = kBlock / kTileRows;   // 16-row tiles per 128-block of h
 
 struct MatDesc {
     CUtensorMap tm_codes;     // uint8 {row bytes, n}, box {128, 16}, 128-byte swizzle; or
@@ -54,7 +57,11 @@ struct KArgs {
     MatDesc mat[3];           // phase A: gate, up; phase B: mat[2]
     int do_a, do_b;
     int slots;                // ring slots
-    uint32_t off_scales, off_act, off_sn, off_part, off_tcnt;   // dynamic smem layout
+    // dynamic shared memory: ring codes | ring scales | phase A activation +
+    // (scale, magic - sum) pairs | phase B activation + pairs | segment sums |
+    // int counters: units per tile, tiles folded, phase B segment state
+    uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt;
+    int tiles_max, nseg_max;
     // phase A input
     int in_mode;
     const uint16_t *x;        // bf16 [M][hidden]                 (kInRotX)
@@ -80,16 +87,23 @@ struct KArgs {
     const float *sb;
     float *y;                 // fp32 [M][nB]
     int32_t *dots;            // int32 [M][nB][kB/128] or null
-    unsigned long long *gbar; // grid barrier arrivals (monotonic)
+    unsigned *segready;       // per 8-block segment of h: its 128-blocks rotated (A+B launches)
+    unsigned *done;           // CTAs finished with phase B (A+B launches); zero on entry and exit
     unsigned *err;            // bit 0: producer wait, 1: producer drain, 2: consumer wait, 4: grid barrier
 };
 
-// Tile range and unit counts of one phase for CTA c of G.
+// The tiles and units of one phase for CTA c of G.  Tiles are dealt out
+// strided: CTA c takes tiles start, start + G, ... with start = c (phase A)
+// or G - 1 - c (phase B), so the CTAs holding one more phase-A tile are not
+// the ones holding one more phase-B tile, and the 128-blocks of h complete
+// evenly over phase A.  Unit order: phase A tile-major (tile, matrix,
+// segment); phase B segment-major (segment, tile), so that a CTA needs the
+// segments of h in the order they become ready.
 struct PhaseGeo {
-    int n, k, nb, nseg, upt, ntiles, t0, t1, units;
+    int n, k, nb, nseg, upt, ntiles, start, count, units;
 };
 
-__host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int c) {
+__host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int c, bool reverse) {
     PhaseGeo p{};
     if (n <= 0) return p;
     p.n = n;
@@ -98,43 +112,27 @@ __host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int
     p.nseg = (p.nb + kSegBlocks - 1) / kSegBlocks;
     p.upt = nmat * p.nseg;
     p.ntiles = (n + kTileRows - 1) / kTileRows;
-    p.t0 = static_cast<int>(static_cast<long long>(p.ntiles) * c / G);
-    p.t1 = static_cast<int>(static_cast<long long>(p.ntiles) * (c + 1) / G);
-    p.units = (p.t1 - p.t0) * p.upt;
+    p.start = reverse ? G - 1 - c : c;
+    p.count = p.start < p.ntiles ? (p.ntiles - 1 - p.start) / G + 1 : 0;
+    p.units = p.count * p.upt;
     return p;
+}
+
+// Largest tile count phase_geo gives any CTA.
+__host__ __device__ inline int phase_tiles_max(int n, int G) {
+    const int ntiles = (n + kTileRows - 1) / kTileRows;
+    return (ntiles + G - 1) / G;
+}
+
+// Fire-and-forget add at gpu scope (nothing waits for a returned value).
+__device__ __forceinline__ void red_add_relaxed_gpu(unsigned *p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid-wide barrier among gridDim.x co-resident CTAs, one thread per CTA:
-// a 64-bit arrival count that only grows, so a barrier is one atomic and a
-// poll until the count reaches the end of this barrier's generation.
-// Bounded: after kWaitBudgetCycles it sets err bit 4 and returns false.
-__device__ __forceinline__ bool grid_barrier(unsigned long long *gbar, unsigned *err) {
-    __threadfence();
-    const unsigned long long G = gridDim.x;
-    const unsigned long long ticket = atomicAdd(gbar, 1ull);
-    const unsigned long long target = (ticket / G + 1) * G;
-    if (ticket + 1 == target) return true;
-    const long long t0 = clock64();
-    while (ld_acquire_u64(gbar) < target) {
-        if (clock64() - t0 > kWaitBudgetCycles) {
-            if (err != nullptr) atomicOr(err, 16u);
-            return false;
-        }
-        __nanosleep(32);
-    }
-    return true;
 }
 
 // (scale, 0x4b400000 - sum q) of one staged block: the second word turns a
@@ -156,60 +154,6 @@ __device__ __forceinline__ int stage_block_lanes(const int8_t q[4], int lane, ui
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     return sum;
-}
-
-// Stage int8 rows q [M][k] (+ fp32 s [M][k/128]) from global memory; each
-// warp loads a group of up to 4 blocks before working on any of them.
-template <int FMT, int M>
-__device__ __forceinline__ void stage_plain(const int8_t *__restrict__ q, const float *__restrict__ s,
-                                            int k, uint8_t *act, float2 *sn, int warp, int lane) {
-    const int nb = k / kBlock;
-    constexpr int kGroup = 4;
-    for (int blk0 = warp; blk0 < M * nb; blk0 += kGroup * kConsumerWarps) {
-        uint32_t w[kGroup];
-        float sc[kGroup];
-#pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-            const int blk = blk0 + u * kConsumerWarps;
-            w[u] = 0u;
-            sc[u] = 0.0f;
-            if (blk < M * nb) {
-                const int r = blk / nb, b = blk - r * nb;
-                w[u] = __ldcg(reinterpret_cast<const unsigned *>(q + static_cast<size_t>(r) * k + static_cast<size_t>(b) * kBlock) + lane);
-                sc[u] = __ldcg(s + static_cast<size_t>(r) * nb + b);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-            const int blk = blk0 + u * kConsumerWarps;
-            if (blk >= M * nb) break;
-            const int r = blk / nb, b = blk - r * nb;
-            uint8_t *dst = act + static_cast<size_t>(b * M + r) * kBlock;
-            int sum = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int v = static_cast<int8_t>(w[u] >> (8 * i));
-                dst[staged_pos<FMT>(4 * lane + i)] = static_cast<uint8_t>(v);
-                sum += v;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (lane == 0) sn[b * M + r] = block_sn(sc[u], sum);
-        }
-    }
-}
-
-// Copy an activation already staged in global memory (nb blocks of 128*M
-// bytes + nb*M (scale, magic - sum) pairs) into shared memory, 16 bytes a
-// thread.
-template <int M>
-__device__ __forceinline__ void stage_copy(const uint8_t *__restrict__ st, const float2 *__restrict__ ssn,
-                                           int nb, uint8_t *act, float2 *sn, int tid) {
-    const int n16 = nb * kBlock * M / 16;
-    const uint4 *src = reinterpret_cast<const uint4 *>(st);
-    uint4 *dst = reinterpret_cast<uint4 *>(act);
-    for (int i = tid; i < n16; i += kConsumers) dst[i] = __ldcg(src + i);
-    for (int i = tid; i < nb * M; i += kConsumers) sn[i] = __ldcg(ssn + i);
 }
 
 // Rotate + quantise rows of bf16 values (in_fn(r, i) gives element i of row
@@ -273,22 +217,20 @@ __device__ __forceinline__ float fold_tree(float *V, int cnt, int stride) {
 // fold step t_b into the segment sums of weight rows g and g+8.
 // One unit: 16 weight rows x the segment's blocks.  Lane l = 16h + r works
 // on row r, half h of every block (2-bit: words 4h..4h+3, 64 weights; 1-bit:
-// words 2h, 2h+1); the halves' dp4a sums meet in one shuffle and lane r
-// (h = 0) folds t_b = (float)d * (ws * sa) into the segment sums acc[mm]
-// in ascending block order.
-template <int FMT, int M, bool DOTS>
+// words 2h, 2h+1); each code word feeds its own dp4a chain, the chains and
+// the two halves meet in adds and one shuffle, and lane r (h = 0) folds
+// t_b = (float)d * (ws * sa) into the segment sums acc[mm] in ascending block
+// order.  dots (may be null) receives every block dot.
+template <int FMT, int M>
 __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
                                           int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
                                           int32_t *dots, int row, int n, int nb) {
     const int r = lane & 15, h = lane >> 4;
-    const int sw = r & 7;                                   // 128-byte swizzle of the row
 #pragma unroll
     for (int bl = 0; bl < kSegBlocks; ++bl) {
         if (bl >= bcount) break;
         const int b = b0 + bl;
         int dot[M];
-#pragma unroll
-        for (int mm = 0; mm < M; ++mm) dot[mm] = 0;
         const uint8_t *ab = act + static_cast<size_t>(b) * M * kBlock + h * 64;
         if constexpr (FMT == 0) {
             // 128-byte line of (row r, plane bl/4): 3D copies lay rows out
@@ -298,6 +240,7 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
             const uint4 cw = *reinterpret_cast<const uint4 *>(cs + line * 128 +
                                                               ((((bl & 3) * 2 + h) ^ (line & 7)) * 16));
             const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            int part[M][4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint32_t p0, p1, p2, p3;
@@ -305,15 +248,18 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
 #pragma unroll
                 for (int mm = 0; mm < M; ++mm) {
                     const uint4 av = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 16);
-                    dot[mm] = __dp4a(static_cast<int>(p0), static_cast<int>(av.x), dot[mm]);
-                    dot[mm] = __dp4a(static_cast<int>(p1), static_cast<int>(av.y), dot[mm]);
-                    dot[mm] = __dp4a(static_cast<int>(p2), static_cast<int>(av.z), dot[mm]);
-                    dot[mm] = __dp4a(static_cast<int>(p3), static_cast<int>(av.w), dot[mm]);
+                    int d = __dp4a(static_cast<int>(p0), static_cast<int>(av.x), 0);
+                    d = __dp4a(static_cast<int>(p1), static_cast<int>(av.y), d);
+                    d = __dp4a(static_cast<int>(p2), static_cast<int>(av.z), d);
+                    part[mm][i] = __dp4a(static_cast<int>(p3), static_cast<int>(av.w), d);
                 }
             }
+#pragma unroll
+            for (int mm = 0; mm < M; ++mm) dot[mm] = (part[mm][0] + part[mm][1]) + (part[mm][2] + part[mm][3]);
         } else {
-            const uint2 cw = *reinterpret_cast<const uint2 *>(cs + r * 128 + ((bl ^ sw) * 16) + h * 8);
+            const uint2 cw = *reinterpret_cast<const uint2 *>(cs + r * 128 + ((bl ^ (r & 7)) * 16) + h * 8);
             const uint32_t words[2] = {cw.x, cw.y};
+            int part[M][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
 #pragma unroll
@@ -321,11 +267,18 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
                     const uint4 a0 = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 32);
                     const uint4 a1 = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 32 + 16);
                     const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    int d0 = 0, d1 = 0;
 #pragma unroll
-                    for (int sb = 0; sb < 8; ++sb)
-                        dot[mm] = __dp4a(static_cast<int>((words[i] >> sb) & 0x01010101u), static_cast<int>(av[sb]), dot[mm]);
+                    for (int sb = 0; sb < 8; sb += 2) {
+                        d0 = __dp4a(static_cast<int>((words[i] >> sb) & 0x01010101u), static_cast<int>(av[sb]), d0);
+                        d1 = __dp4a(static_cast<int>((words[i] >> (sb + 1)) & 0x01010101u), static_cast<int>(av[sb + 1]), d1);
+                    }
+                    part[mm][2 * i] = d0;
+                    part[mm][2 * i + 1] = d1;
                 }
             }
+#pragma unroll
+            for (int mm = 0; mm < M; ++mm) dot[mm] = (part[mm][0] + part[mm][1]) + (part[mm][2] + part[mm][3]);
         }
         const uint32_t wsw = wsr[bl >> 1];
         const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
@@ -336,9 +289,120 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
             const float2 sv = sn[b * M + mm];                // (activation scale, magic - sum q)
             const float v = int_to_float_exact(d, __float_as_int(sv.y));
             acc[mm] = __fadd_rn(acc[mm], __fmul_rn(v, __fmul_rn(ws, sv.x)));
-            if constexpr (DOTS)
-                if (h == 0 && row < n) dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
+            if (dots != nullptr && h == 0 && row < n) dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
         }
+    }
+}
+
+// Stage blocks [b_begin, b_end) of int8 rows q [M][k] (+ fp32 s [M][k/128])
+// from global memory, warps w, w + nw, ... taking (row, block) pairs; each
+// warp loads a group of up to 4 blocks before working on any of them.
+template <int FMT, int M>
+__device__ __forceinline__ void stage_plain_range(const int8_t *__restrict__ q, const float *__restrict__ s, int k,
+                                                  int b_begin, int b_end, uint8_t *act, float2 *sn, int w, int nw,
+                                                  int lane) {
+    const int nb = k / kBlock, cnt = b_end - b_begin;
+    constexpr int kGroup = 4;
+    for (int p0 = w; p0 < M * cnt; p0 += kGroup * nw) {
+        uint32_t wd[kGroup];
+        float sc[kGroup];
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            const int p = p0 + u * nw;
+            wd[u] = 0u;
+            sc[u] = 0.0f;
+            if (p < M * cnt) {
+                const int r = p / cnt, b = b_begin + (p - r * cnt);
+                wd[u] = __ldcg(reinterpret_cast<const unsigned *>(q + static_cast<size_t>(r) * k + static_cast<size_t>(b) * kBlock) + lane);
+                sc[u] = __ldcg(s + static_cast<size_t>(r) * nb + b);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            const int p = p0 + u * nw;
+            if (p >= M * cnt) break;
+            const int r = p / cnt, b = b_begin + (p - r * cnt);
+            uint8_t *dst = act + static_cast<size_t>(b * M + r) * kBlock;
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int v = static_cast<int8_t>(wd[u] >> (8 * i));
+                dst[staged_pos<FMT>(4 * lane + i)] = static_cast<uint8_t>(v);
+                sum += v;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) sn[b * M + r] = block_sn(sc[u], sum);
+        }
+    }
+}
+
+// Make segment j of phase B's activation present in shared memory.  The
+// first warp to need it stages it (after, in a launch that also runs phase
+// A, the segment's 128-blocks of h have all been rotated somewhere on the
+// GPU); other warps wait for it.  Returns false if a bounded wait ran out.
+template <int FMT, int M>
+__device__ bool stage_segment_b(const KArgs &a, const PhaseGeo &P, int j, uint8_t *act_h, float2 *sn_h,
+                                int *segst, int lane) {
+    volatile int *vst = segst;
+    if (vst[j] == 2) {
+        __threadfence_block();
+        return true;
+    }
+    int claim = 0;
+    if (lane == 0) claim = atomicCAS(&segst[j], 0, 1) == 0;
+    claim = __shfl_sync(0xffffffffu, claim, 0);
+    const int b0 = j * kSegBlocks, bc = min(kSegBlocks, P.nb - b0);
+    int ok = 1;
+    if (claim) {
+        if (a.do_a && lane == 0) {
+            const long long t0 = clock64();
+            while (ld_acquire_u32(a.segready + j) < static_cast<unsigned>(bc)) {
+                if (clock64() - t0 > kWaitBudgetCycles) {
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (a.bst != nullptr) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.bst + static_cast<size_t>(b0) * M * kBlock);
+            uint4 *dst = reinterpret_cast<uint4 *>(act_h + static_cast<size_t>(b0) * M * kBlock);
+            for (int i = lane; i < bc * M * kBlock / 16; i += 32) dst[i] = __ldcg(src + i);
+            for (int i = lane; i < bc * M; i += 32) sn_h[b0 * M + i] = __ldcg(a.bsn + b0 * M + i);
+        } else {
+            stage_plain_range<FMT, M>(a.qb, a.sb, P.k, b0, b0 + bc, act_h, sn_h, 0, 1, lane);
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) atomicExch(&segst[j], 2);
+    } else if (lane == 0) {
+        const long long t0 = clock64();
+        while (vst[j] != 2) {
+            if (clock64() - t0 > kWaitBudgetCycles) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __threadfence_block();
+    return ok != 0;
+}
+
+// Decoded position of a phase's unit: phase A (outer = tile, inner = matrix
+// x segment), phase B (outer = segment, inner = tile); inner runs fastest.
+struct UnitPos {
+    int outer, inner;
+};
+
+__device__ __forceinline__ void unit_advance(UnitPos &u, int step, int extent) {
+    u.inner += step;
+    while (u.inner >= extent) {
+        u.inner -= extent;
+        ++u.outer;
     }
 }
 
@@ -355,13 +419,20 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *codes_ring = base;
     const uint16_t *scales_ring = reinterpret_cast<const uint16_t *>(base + a.off_scales);
-    uint8_t *act = base + a.off_act;
-    float2 *sn = reinterpret_cast<float2 *>(base + a.off_sn);
+    uint8_t *act_x = base + a.off_act;
+    float2 *sn_x = reinterpret_cast<float2 *>(base + a.off_sn);
+    uint8_t *act_h = base + a.off_acth;
+    float2 *sn_h = reinterpret_cast<float2 *>(base + a.off_snh);
     float *part = reinterpret_cast<float *>(base + a.off_part);
+    // int counters: units done per local tile of phase A, of phase B; phase A
+    // tiles folded; phase B segments (0 absent, 1 staging, 2 staged)
     int *tcnt = reinterpret_cast<int *>(base + a.off_tcnt);
+    int *tdone = tcnt + 2 * a.tiles_max;
+    int *segst = tdone + a.tiles_max;
 
-    const PhaseGeo ga = a.do_a ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta) : PhaseGeo{};
-    const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta) : PhaseGeo{};
+    const PhaseGeo ga = a.do_a ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta, false) : PhaseGeo{};
+    const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta, true) : PhaseGeo{};
+    const int total = ga.units + gb.units;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -370,40 +441,41 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
         }
         mbar_init_fence();
     }
+    for (int i = threadIdx.x; i < 3 * a.tiles_max + a.nseg_max; i += kThreads) tcnt[i] = 0;
     __syncthreads();
     pdl_launch_dependents();
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        // units in order: phase A (tile, gate/up, segment), then phase B
-        // (tile, segment).  Lanes 0..kProducerLanes-1 each issue every
-        // kProducerLanes-th unit, so several units are in the issue pipe at
-        // once; (lt, ru) and (slot, round) = divmod(k, S) advance incrementally.
+        // Lanes 0..kProducerLanes-1 each issue every kProducerLanes-th unit,
+        // so several units are in the issue pipe at once; unit positions and
+        // (slot, round) = divmod(k, S) advance incrementally.
         constexpr int kProducerLanes = 4;
-        const int total = ga.units + gb.units;
         if (lane < kProducerLanes) {
             bool ok = true;
             int k = lane;
             bool in_a = k < ga.units;
-            int lt, ru;
-            {
-                const int i0 = in_a ? k : k - ga.units;
-                const int upt = in_a ? ga.upt : max(gb.upt, 1);
-                lt = i0 / upt;
-                ru = i0 - lt * upt;
-            }
+            UnitPos u{0, in_a ? k : k - ga.units};
+            unit_advance(u, 0, in_a ? max(ga.upt, 1) : max(gb.count, 1));
             int slot = k % S, round = k / S;
             for (; k < total && ok; k += kProducerLanes) {
                 if (in_a && k >= ga.units) {
                     in_a = false;
-                    const int i0 = k - ga.units;
-                    lt = i0 / gb.upt;
-                    ru = i0 - lt * gb.upt;
+                    u = UnitPos{0, k - ga.units};
+                    unit_advance(u, 0, gb.count);
                 }
                 const PhaseGeo &P = in_a ? ga : gb;
-                const int mi = in_a ? (ru >= P.nseg ? 1 : 0) : 2;
-                const int seg = in_a && ru >= P.nseg ? ru - P.nseg : ru;
-                const int tile = P.t0 + lt;
+                int mi, seg, lt;
+                if (in_a) {
+                    lt = u.outer;
+                    mi = u.inner >= P.nseg ? 1 : 0;
+                    seg = u.inner - mi * P.nseg;
+                } else {
+                    seg = u.outer;
+                    lt = u.inner;
+                    mi = 2;
+                }
+                const int tile = P.start + lt * G;
                 const MatDesc &md = a.mat[mi];
                 if (round > 0 && !(ok = mbar_wait(smem_u32(&empty_bar[slot]), (round - 1) & 1))) break;
                 const uint32_t fb = smem_u32(&full_bar[slot]);
@@ -422,11 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 if (sct)
                     tma_load_2d(smem_u32(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2)), &md.tm_scales,
                                 seg * kSegBlocks, tile * kTileRows, fb);
-                ru += kProducerLanes;
-                while (ru >= P.upt) {
-                    ru -= P.upt;
-                    ++lt;
-                }
+                unit_advance(u, kProducerLanes, in_a ? P.upt : P.count);
                 slot += kProducerLanes;
                 if (slot >= S) {
                     slot -= S;
@@ -456,71 +524,84 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     bool ok = true;
     pdl_wait();
 
-    for (int ph = 0; ph < 2; ++ph) {
-        const bool is_a = ph == 0;
-        if (is_a ? !a.do_a : !a.do_b) continue;
-        const PhaseGeo &P = is_a ? ga : gb;
-        const int kbase = is_a ? 0 : ga.units;
-
-        // ---- stage this phase's activation
-        if (is_a) {
-            if (a.in_mode == kInRotX) {
-                const uint16_t *x = a.x;
-                const int hidden = P.k;
-                stage_rotated<FMT, M>([&](int r, int i) { return bf16_bits_to_f32(x[static_cast<size_t>(r) * hidden + i]); },
-                                      P.k, act, sn, warp, lane, cta == 0 ? a.qx : nullptr, a.sx);
-            } else if (a.in_mode == kInNormY) {
-                const int hidden = P.k;
-                for (int r = 0; r < M; ++r) {
-                    // 1/rms: 256 partial sums (thread i adds y[i], y[i+256], ...),
-                    // each warp's 32 combined at distance 1, 2, ..., 16, then
-                    // ((w0+w1)+(w2+w3)) + ((w4+w5)+(w6+w7))
-                    const float *yr = a.y_in + static_cast<size_t>(r) * hidden;
-                    float acc = 0.0f;
-                    if (tid < 256)
-                        for (int i = tid; i < hidden; i += 256) {
-                            const float v = __ldcg(yr + i);
-                            acc = __fadd_rn(acc, __fmul_rn(v, v));
-                        }
+    // ---- phase A's activation: every CTA rotates + quantises the input
+    if (a.do_a) {
+        const int hidden = ga.k;
+        if (a.in_mode == kInRotX) {
+            const uint16_t *x = a.x;
+            stage_rotated<FMT, M>([&](int r, int i) { return bf16_bits_to_f32(x[static_cast<size_t>(r) * hidden + i]); },
+                                  hidden, act_x, sn_x, warp, lane, cta == 0 ? a.qx : nullptr, a.sx);
+        } else if (a.in_mode == kInNormY) {
+            for (int r = 0; r < M; ++r) {
+                // 1/rms: 256 partial sums (thread i adds y[i], y[i+256], ...),
+                // each warp's 32 combined at distance 1, 2, ..., 16, then
+                // ((w0+w1)+(w2+w3)) + ((w4+w5)+(w6+w7))
+                const float *yr = a.y_in + static_cast<size_t>(r) * hidden;
+                float acc = 0.0f;
+                if (tid < 256)
+                    for (int i = tid; i < hidden; i += 256) {
+                        const float v = __ldcg(yr + i);
+                        acc = __fadd_rn(acc, __fmul_rn(v, v));
+                    }
 #pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-                    if (lane == 0 && warp < 8) s_warp[warp] = acc;
-                    named_barrier(1, kConsumers);
-                    const float w01 = __fadd_rn(s_warp[0], s_warp[1]), w23 = __fadd_rn(s_warp[2], s_warp[3]);
-                    const float w45 = __fadd_rn(s_warp[4], s_warp[5]), w67 = __fadd_rn(s_warp[6], s_warp[7]);
-                    const float ss = __fadd_rn(__fadd_rn(w01, w23), __fadd_rn(w45, w67));
-                    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hidden)), a.eps)));
-                    named_barrier(1, kConsumers);
-                    stage_rotated<FMT, M>([&](int, int i) {
-                        return bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__ldcg(yr + i), inv)));
-                    }, hidden, act, sn, warp, lane, cta == 0 ? a.qx : nullptr, a.sx, r);
-                }
-            } else {
-                stage_plain<FMT, M>(a.qa, a.sa, P.k, act, sn, warp, lane);
+                for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+                if (lane == 0 && warp < 8) s_warp[warp] = acc;
+                named_barrier(1, kConsumers);
+                const float w01 = __fadd_rn(s_warp[0], s_warp[1]), w23 = __fadd_rn(s_warp[2], s_warp[3]);
+                const float w45 = __fadd_rn(s_warp[4], s_warp[5]), w67 = __fadd_rn(s_warp[6], s_warp[7]);
+                const float ss = __fadd_rn(__fadd_rn(w01, w23), __fadd_rn(w45, w67));
+                const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hidden)), a.eps)));
+                named_barrier(1, kConsumers);
+                stage_rotated<FMT, M>([&](int, int i) {
+                    return bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__ldcg(yr + i), inv)));
+                }, hidden, act_x, sn_x, warp, lane, cta == 0 ? a.qx : nullptr, a.sx, r);
             }
-        } else if (a.bst != nullptr) {
-            stage_copy<M>(a.bst, a.bsn, P.nb, act, sn, tid);
         } else {
-            stage_plain<FMT, M>(a.qb, a.sb, P.k, act, sn, warp, lane);
+            stage_plain_range<FMT, M>(a.qa, a.sa, hidden, 0, ga.nb, act_x, sn_x, warp, kConsumerWarps, lane);
         }
-        for (int i = tid; i < P.t1 - P.t0; i += kConsumers) tcnt[i] = 0;
         named_barrier(1, kConsumers);
+    }
 
-        // ---- units of this phase: CTA-local index k, compute warp k % 14;
-        // (lt, ru) = divmod(k - kbase, upt) and (slot, round) = divmod(k, S)
-        // advance incrementally.  A compute warp never waits on anything but
-        // its data: tile epilogues run on the epilogue warp.
-        if (warp < kComputeWarps) {
-        int k = kbase + ((warp - kbase) % kComputeWarps + kComputeWarps) % kComputeWarps;
-        int lt = (k - kbase) / max(P.upt, 1), ru = (k - kbase) - lt * P.upt;
+    // ---- units: CTA-local index k over phase A then phase B, compute warp
+    // k % ncw.  A compute warp waits only for its data (and, in phase B, for
+    // the segment of h it needs); h-block bookkeeping runs on the epilogue
+    // warp, which computes units too when there is none.
+    const bool epi = a.do_a && a.rotate_h;
+    const int ncw = epi ? kComputeWarps : kConsumerWarps;
+    int *tcnt_a = tcnt, *tcnt_b = tcnt + a.tiles_max;
+    float *part_a = part, *part_b = part + static_cast<size_t>(ga.units) * M * kTileRows;
+    if (warp < ncw) {
+        int k = warp;
+        bool in_a = k < ga.units;
+        UnitPos u{0, in_a ? k : k - ga.units};
+        unit_advance(u, 0, in_a ? max(ga.upt, 1) : max(gb.count, 1));
         int slot = k % S, round = k / S;
-        for (; k < kbase + P.units; k += kComputeWarps) {
+        int staged_seg = -1;
+        for (; k < total; k += ncw) {
+            if (in_a && k >= ga.units) {
+                in_a = false;
+                u = UnitPos{0, k - ga.units};
+                unit_advance(u, 0, gb.count);
+            }
+            const PhaseGeo &P = in_a ? ga : gb;
+            int mi, seg, lt;
+            if (in_a) {
+                lt = u.outer;
+                mi = u.inner >= P.nseg ? 1 : 0;
+                seg = u.inner - mi * P.nseg;
+            } else {
+                seg = u.outer;
+                lt = u.inner;
+                mi = 2;
+                if (seg != staged_seg) {
+                    if (!stage_segment_b<FMT, M>(a, P, seg, act_h, sn_h, segst, lane)) ok = false;
+                    staged_seg = seg;
+                }
+            }
+            const int i = in_a ? k : k - ga.units;          // unit index within its phase
             if (ok && !mbar_wait(smem_u32(&full_bar[slot]), round & 1)) ok = false;
             if (!ok) break;
-            const int i = k - kbase;
-            const int mi = is_a ? (ru >= P.nseg ? 1 : 0) : 2;
-            const int seg = is_a && ru >= P.nseg ? ru - P.nseg : ru;
-            const int tile = P.t0 + lt;
+            const int tile = P.start + lt * G;
             const MatDesc &md = a.mat[mi];
             const uint8_t *cs = codes_ring + static_cast<size_t>(slot) * kCodesSlot;
             const int bcount = min(kSegBlocks, P.nb - seg * kSegBlocks);
@@ -546,125 +627,174 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             float acc[M];
 #pragma unroll
             for (int mm = 0; mm < M; ++mm) acc[mm] = 0.0f;
-            if (!is_a && a.dots != nullptr)
-                unit_dp4a<FMT, M, true>(cs, md.codes3d != 0, act, sn, seg * kSegBlocks, bcount, wsr, lane, acc, a.dots, row, P.n, P.nb);
-            else
-                unit_dp4a<FMT, M, false>(cs, md.codes3d != 0, act, sn, seg * kSegBlocks, bcount, wsr, lane, acc, nullptr, row, P.n, P.nb);
+            unit_dp4a<FMT, M>(cs, md.codes3d != 0, in_a ? act_x : act_h, in_a ? sn_x : sn_h, seg * kSegBlocks,
+                              bcount, wsr, lane, acc, in_a ? nullptr : a.dots, row, P.n, P.nb);
             // the slot's codes and scales are all in registers: hand it back
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-            // advance to this warp's next unit
-            const int lt_done = lt;
-            ru += kComputeWarps;
-            while (ru >= P.upt) {
-                ru -= P.upt;
-                ++lt;
-            }
-            slot += kComputeWarps;
+            unit_advance(u, ncw, in_a ? P.upt : P.count);
+            slot += ncw;
             while (slot >= S) {
                 slot -= S;
                 ++round;
             }
 
             // segment sums of this unit -> shared memory; count the tile
-            float *pu = part + static_cast<size_t>(i) * M * kTileRows;
+            float *pu = (in_a ? part_a : part_b) + static_cast<size_t>(i) * M * kTileRows;
             if (lane < kTileRows) {
 #pragma unroll
                 for (int mm = 0; mm < M; ++mm) pu[mm * kTileRows + lane] = acc[mm];
             }
             __syncwarp();
+            int last = 0;
             if (lane == 0) {
                 __threadfence_block();
-                atomicAdd(&tcnt[lt_done], 1);
+                last = atomicAdd(&(in_a ? tcnt_a : tcnt_b)[lt], 1) == P.upt - 1;
             }
-        }
-        } else {
-        // ---- epilogue warp: tiles in order, each once all its units are in
-        const volatile int *vt = tcnt;
-        for (int lt_done = 0; lt_done < P.t1 - P.t0; ++lt_done) {
-            const long long w0 = clock64();
-            while (vt[lt_done] < P.upt) {
-                if (clock64() - w0 > kWaitBudgetCycles) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(32);
-            }
-            if (!ok) break;
+            if (!__shfl_sync(0xffffffffu, last, 0)) continue;
             __threadfence_block();
-            const int tile = P.t0 + lt_done;
-            const int rr16 = lane & 15;
-            const int row = tile * kTileRows + rr16;
 
-            // ---- tile epilogue: fold the segment sums with the pairwise tree
+            // ---- the tile's last unit: fold its segment sums with the pairwise
+            // tree and store h (phase A) or y (phase B); no global fence here.
+            // Phase A units of a tile are consecutive; phase B's are `count` apart.
             const int r = lane >> 4;            // activation rows r, r + 2, ... of the tile's 16 outputs
-            float *pt = part + static_cast<size_t>(lt_done) * P.upt * M * kTileRows + r * kTileRows + rr16;
-            if (is_a) {
-                for (int ra = r; ra < M; ra += 2) {
-                    float *pr = pt + (ra - r) * kTileRows;
-                    const float gv = fold_tree(pr, P.nseg, M * kTileRows);
-                    const float uv = fold_tree(pr + static_cast<size_t>(P.nseg) * M * kTileRows, P.nseg, M * kTileRows);
+            const size_t ustride = static_cast<size_t>(in_a ? 1 : P.count) * M * kTileRows;
+            float *pt = (in_a ? part_a + static_cast<size_t>(lt) * P.upt * M * kTileRows : part_b + static_cast<size_t>(lt) * M * kTileRows) +
+                        r * kTileRows + rr16;
+            for (int ra = r; ra < M; ra += 2) {
+                float *pr = pt + (ra - r) * kTileRows;
+                if (in_a) {
+                    const float gv = fold_tree(pr, P.nseg, static_cast<int>(ustride));
+                    const float uv = fold_tree(pr + P.nseg * ustride, P.nseg, static_cast<int>(ustride));
                     if (row < P.n)
                         a.h[static_cast<size_t>(ra) * P.n + row] = f32_to_bf16_bits(__fmul_rn(tq_silu(gv), uv));
-                }
-                if (a.rotate_h) {
-                    // the CTA completing the last tile of a 128-block of h rotates it
-                    __syncwarp();
-                    const int hb = tile * kTileRows / kBlock;
-                    const unsigned add = static_cast<unsigned>(min(kTileRows, P.n - tile * kTileRows));
-                    int hlast = 0;
-                    if (lane == 0) {
-                        __threadfence();
-                        hlast = atomicAdd(&a.hcount[hb], add) + add == static_cast<unsigned>(kBlock);
-                    }
-                    hlast = __shfl_sync(0xffffffffu, hlast, 0);
-                    if (hlast) {
-                        __threadfence();
-                        const int nbh = P.n / kBlock;
-                        float v[M][4];
-#pragma unroll
-                        for (int rr = 0; rr < M; ++rr)
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc)
-                                v[rr][cc] = bf16_bits_to_f32(__ldcg(a.h + static_cast<size_t>(rr) * P.n + hb * kBlock + lane + 32 * cc));
-#pragma unroll
-                        for (int rr = 0; rr < M; ++rr) wht128_warp(v[rr], lane);
-#pragma unroll
-                        for (int rr = 0; rr < M; ++rr) {
-                            int8_t q[4];
-                            const float sc = quant_block_warp(v[rr], q);
-                            int sum = 0;
-                            uint8_t *hst = a.hst + static_cast<size_t>(hb * M + rr) * kBlock;
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) {
-                                const int e = lane + 32 * cc;
-                                a.qh[static_cast<size_t>(rr) * P.n + hb * kBlock + e] = q[cc];
-                                hst[staged_pos<FMT>(e)] = static_cast<uint8_t>(q[cc]);
-                                sum += q[cc];
-                            }
-#pragma unroll
-                            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                            if (lane == 0) {
-                                a.sh[static_cast<size_t>(rr) * nbh + hb] = sc;
-                                a.hsn[hb * M + rr] = block_sn(sc, sum);
-                            }
-                        }
-                        if (lane == 0) a.hcount[hb] = 0u;
-                    }
-                }
-            } else {
-                for (int ra = r; ra < M; ra += 2) {
-                    const float yv = fold_tree(pt + (ra - r) * kTileRows, P.nseg, M * kTileRows);
+                } else {
+                    const float yv = fold_tree(pr, P.nseg, static_cast<int>(ustride));
                     if (row < P.n) a.y[static_cast<size_t>(ra) * P.n + row] = yv;
                 }
             }
+            if (in_a && epi) {
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    atomicExch(&tdone[lt], 1);
+                }
+            }
         }
+    } else if (epi) {
+        // ---- epilogue warp: publish each folded phase-A tile into its
+        // 128-block of h with a gpu-scope fence and a fire-and-forget add of
+        // its rows.  The CTA holding a block's last tile owns the block: after
+        // publishing that tile it waits for the block's 128 rows, rotates and
+        // quantises it, and (when this launch runs phase B) counts it into its
+        // segment's ready counter.
+        // Tiles are published in batches (every tile folded so far, behind one
+        // fence, one add per tile); an owned block is rotated as soon as its
+        // 128 rows are in, checked without blocking so that a late CTA never
+        // holds up this CTA's own publishing.  pend: owned tiles (bit lt)
+        // whose block still waits.
+        const volatile int *vd = tdone;
+        int lt = 0;
+        unsigned pend = 0u;
+        const long long w0 = clock64();
+        while ((lt < ga.count || pend != 0u) && ok) {
+            bool progress = false;
+            if (lt < ga.count && vd[lt] != 0) {
+                int lt_end = lt + 1;
+                while (lt_end < ga.count && lt_end - lt < 32 && vd[lt_end] != 0) ++lt_end;
+                __syncwarp();
+                __threadfence();
+                if (lane < lt_end - lt) {
+                    const int tile = ga.start + (lt + lane) * G;
+                    red_add_relaxed_gpu(&a.hcount[tile / kTilesPerHBlock],
+                                        static_cast<unsigned>(min(kTileRows, ga.n - tile * kTileRows)));
+                }
+                for (; lt < lt_end; ++lt) {
+                    const int tile = ga.start + lt * G;
+                    const int hb = tile / kTilesPerHBlock;
+                    if (tile == min((hb + 1) * kTilesPerHBlock, ga.ntiles) - 1) pend |= 1u << lt;
+                }
+                progress = true;
+            }
+            int own = -1;
+            if (pend != 0u) {
+                // the first pending owned block whose rows are all in, if any
+                int found = -1;
+                if (lane == 0) {
+                    for (unsigned m = pend; m != 0u; m &= m - 1u) {
+                        const int l = __ffs(m) - 1;
+                        const int hb = (ga.start + l * G) / kTilesPerHBlock;
+                        if (ld_acquire_u32(&a.hcount[hb]) == static_cast<unsigned>(kBlock)) {
+                            found = l;
+                            break;
+                        }
+                    }
+                }
+                own = __shfl_sync(0xffffffffu, found, 0);
+            }
+            if (own < 0) {
+                if (!progress) {
+                    if (clock64() - w0 > kWaitBudgetCycles) ok = false;
+                    __nanosleep(32);
+                }
+                continue;
+            }
+            pend &= ~(1u << own);
+            const int hb = (ga.start + own * G) / kTilesPerHBlock;
+            const int nbh = ga.n / kBlock;
+            float v[M][4];
+#pragma unroll
+            for (int rr = 0; rr < M; ++rr)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    v[rr][cc] = bf16_bits_to_f32(__ldcg(a.h + static_cast<size_t>(rr) * ga.n + hb * kBlock + lane + 32 * cc));
+#pragma unroll
+            for (int rr = 0; rr < M; ++rr) wht128_warp(v[rr], lane);
+#pragma unroll
+            for (int rr = 0; rr < M; ++rr) {
+                int8_t q[4];
+                const float sc = quant_block_warp(v[rr], q);
+                int sum = 0;
+                uint8_t *hst = a.hst + static_cast<size_t>(hb * M + rr) * kBlock;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int e = lane + 32 * cc;
+                    a.qh[static_cast<size_t>(rr) * ga.n + hb * kBlock + e] = q[cc];
+                    hst[staged_pos<FMT>(e)] = static_cast<uint8_t>(q[cc]);
+                    sum += q[cc];
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if (lane == 0) {
+                    a.sh[static_cast<size_t>(rr) * nbh + hb] = sc;
+                    a.hsn[hb * M + rr] = block_sn(sc, sum);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                a.hcount[hb] = 0u;
+                if (a.do_b) {
+                    __threadfence();
+                    red_add_relaxed_gpu(a.segready + hb / kSegBlocks, 1u);
+                }
+            }
         }
+    }
+
+    // ---- a launch running both phases: the last CTA to finish resets the
+    // segment ready counters (no CTA reads them any more)
+    if (a.do_a && a.do_b && a.rotate_h) {
         named_barrier(1, kConsumers);
-        if (is_a && a.do_b) {
-            // every CTA's h blocks are rotated before phase B reads them
-            if (tid == 0 && !grid_barrier(a.gbar, a.err)) ok = false;
-            named_barrier(1, kConsumers);
+        if (warp == 0) {
+            if (lane == 0) {
+                __threadfence();
+                if (atomicAdd(a.done, 1u) == static_cast<unsigned>(G - 1)) {
+                    for (int j = 0; j < gb.nseg; ++j) a.segready[j] = 0u;
+                    *a.done = 0u;
+                    __threadfence();
+                }
+            }
+            __syncwarp();
         }
     }
     if (!ok && lane == 0 && a.err != nullptr) atomicOr(a.err, 4u);

@@ -1,6 +1,6 @@
 // tq_kernel_launch.h -- host interface of the persistent GEMV / FFN kernel
 // (tq_kernel.cuh): one launch runs phase A (gate/up), phase B (down or a
-// plain GEMV), or both with a grid barrier between them, for m <= 4 rows.
+// plain GEMV), or both in one launch, for m <= 4 rows.
 #pragma once
 
 #include <cstddef>
@@ -42,7 +42,8 @@ struct Call {
     const float *sb;
     float *y;
     int32_t *dots;
-    unsigned long long *gbar;
+    unsigned *segready;                 // per segment of h: rotated 128-blocks (A+B launches)
+    unsigned *done;
     unsigned *err;
 };
 

@@ -20,7 +20,7 @@ constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // The FFN workspace at the largest sizes, laid out as tq_ffn_step lays it out
 // (every section 256-byte aligned): qx, sx, h, qh, sh, counters, ybuf, err,
-// grid-barrier count, staged h and its (scale, -sum) pairs.
+// sync counters, staged h and its (scale, magic - sum) pairs.
 constexpr size_t kStaticBytes =
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden) +
     align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxHidden / 128) * 4) +
@@ -28,7 +28,8 @@ constexpr size_t kStaticBytes =
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
     align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 4) +
     align256(static_cast<size_t>(kStaticMaxInter / 128) * 4) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden * 4) + align256(4) + align256(8) +
+    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden * 4) + align256(4) +
+    align256(static_cast<size_t>(2 + kStaticMaxInter / 1024) * 4) +
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
     align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 8);
 

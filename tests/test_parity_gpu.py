@@ -202,9 +202,9 @@ def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
     cnt = wsn[o["counters"]:o["counters"] + 4 * (inter // 128)].view(np.uint32)
     assert np.all(cnt == 0)
     assert wsn[o["err"]:o["err"] + 4].view(np.uint32)[0] == 0     # no wait ran out
-    # the grid barrier's arrival count only grows, by one per CTA per barrier
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert wsn[o["gbar"]:o["gbar"] + 8].view(np.uint64)[0] % sms == 0
+    # the CTA-done count and the per-segment ready counters return to zero
+    nsync = 2 + (inter + 1023) // 1024
+    assert np.all(wsn[o["sync"]:o["sync"] + 4 * nsync].view(np.uint32) == 0)
     g, u, d = mats
     ws2 = tq.ffn_workspace(m, hidden, inter)
     y2 = torch.empty((m, hidden), dtype=torch.float32, device="cuda")
