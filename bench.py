@@ -43,11 +43,6 @@ def layer_bytes(hidden: int, inter: int, fmt: int) -> int:
     return 3 * one
 
 
-def gateup_bytes(hidden: int, inter: int, fmt: int) -> int:
-    per = 4 if fmt == 0 else 8
-    return 2 * (inter * hidden // per + 2 * inter * (hidden // BLOCK))
-
-
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -263,29 +258,16 @@ def run_ours(args, rank, world, local):
                           "tokens_per_s": round(m * 1e6 / us, 1),
                           "hbm_frac": round(lb / us / 1e3 / peak, 4)}
 
-    # --- roofline: the dominant kernel (fused gate/up GEMV + h rotation) of the
-    #     step, launched through the stage entry points with events around it ---
-    gu_bytes = gateup_bytes(HIDDEN, INTER, fmt)
-    ws_r = tq.ffn_workspace(1, HIDDEN, INTER)
-    n_gu = max(N_SETS, min(steps, 4000))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_gu)]
-    for i in range(2 * N_SETS):
-        g, u, d = layers[i % N_SETS]
-        tq.ffn_stage_input(xs[1], INTER, ws_r)
-        tq.ffn_stage_gateup(g, u, 1, ws_r)
-        tq.ffn_stage_down(d, 1, ys[1], ws_r)
-    torch.cuda.synchronize()
-    for i, (e0, e1) in enumerate(evs):
-        g, u, d = layers[i % N_SETS]
-        tq.ffn_stage_input(xs[1], INTER, ws_r)
-        e0.record()
-        tq.ffn_stage_gateup(g, u, 1, ws_r)
-        e1.record()
-        tq.ffn_stage_down(d, 1, ys[1], ws_r)
-    torch.cuda.synchronize()
-    gu_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
-    gu_achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    # --- roofline: at m = 1 the step is one launch of the persistent step
+    #     kernel (tq_kernel<0,1>: gate/up, SiLU*up, rotation of h, down), so the
+    #     dominant kernel's average launch duration is the headline's timed
+    #     region over its launches (CUDA events on the replaying stream).  The
+    #     figure includes the gap between consecutive launches, so `achieved`
+    #     is a lower bound.  Algorithmic bytes per launch: the layer's codes and
+    #     scales, each read once. ---
+    launches = steps                         # one kernel launch per m = 1 step
+    k_us = ms * 1e3 / launches
+    k_achieved = lb / (k_us * 1e-6) / 1e9
 
     # --- end to end through the public API with pinned host buffers: every step
     #     copies x host->device, runs the step, copies y device->host.  The
@@ -361,21 +343,39 @@ def run_ours(args, rank, world, local):
         "hbm_frac": round(value / world / peak, 4),
         "sweep": sweep,
         "roofline": {"bound": "hbm",
-                     "kernel": "gemv_kernel<0,1,true,2,2> (fused gate/up + SiLU*up + h rotation)",
-                     "achieved": round(gu_achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gu_achieved / peak, 4), "peak_kind": peak_kind,
-                     "bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_ms * 1e3, 3),
-                     "traffic": recorded_traffic("gateup_m1")},
+                     "kernel": "tq_kernel<0,1> (whole FFN step: gate/up + SiLU*up + h rotation + down)",
+                     "achieved": round(k_achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(k_achieved / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_launch": lb, "avg_launch_us": round(k_us, 3),
+                     "launches_timed": launches,
+                     "traffic": recorded_traffic("step_m1")},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
                 "how": "pinned H2D copy + tq_ffn_step + D2H copy per step, graph-replayed",
                 "eager_us_per_step": round(eager_ms * 1e3, 3)},
         "stack": stacks,
-        "gpu_launches": steps * 3,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     return result
+
+
+def profile_steps(n: int):
+    """n eager m = 1 steps over the weight sets (no timing, no JSON line)."""
+    import torch
+    from ternary_weight_dp4a_gb300 import build as tqbuild
+    from ternary_weight_dp4a_gb300 import synth, tq
+    tqbuild.build()
+    tq.load()
+    layers = make_weights(tq.FMT_TERNARY2, N_SETS, HIDDEN, INTER)
+    x = synth.activation(1, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
+    y = torch.empty((1, HIDDEN), dtype=torch.float32, device="cuda")
+    ws = tq.ffn_workspace(1, HIDDEN, INTER)
+    for i in range(n):
+        g, u, d = layers[i % N_SETS]
+        tq.ffn_step(g, u, d, x, y=y, workspace=ws)
+    torch.cuda.synchronize()
 
 
 def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1):
@@ -414,6 +414,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--stack-reps", type=int, default=100)
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many eager steps of the headline workload and exit "
+                         "(a small, untimed case for a profiler to capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -439,6 +442,9 @@ def main():
         return
 
     rank, world, local = dist_setup()
+    if args.profile_steps > 0:
+        profile_steps(args.profile_steps)
+        return
     result = run_ours(args, rank, world, local)
     if rank == 0:
         result["cpu_baseline"] = cpu_oracle_baseline(args.cpu_budget)

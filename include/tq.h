@@ -149,19 +149,23 @@ tq_status tq_ffn_workspace_init(void *workspace, size_t workspace_bytes, tq_stre
  * x: bf16 bits [m][hidden], 16-byte aligned.  y: fp32 [m][hidden].
  * workspace: >= tq_ffn_workspace_bytes(m, hidden, inter) bytes, 256-byte
  * aligned, initialised once by tq_ffn_workspace_init; it holds the step's
- * intermediates (qx, sx, h, qh, sh) and the per-block completion counters of
- * h, which every call leaves at zero.  Calls sharing a workspace must not run
+ * intermediates (qx, sx, h, qh, sh, the per-block partial dots of h) and the
+ * per-block and per-segment completion counters of h, which every call leaves
+ * at zero.  Calls sharing a workspace must not run
  * concurrently.
- * The step runs as three kernels (rotate x; gate/up + SiLU*up, whose last CTA
- * per 128-block of h rotates and quantises that block; down), each launched
- * with programmatic stream serialisation: a kernel may start while earlier
- * work in the stream drains, prefetching its weight matrices into L2, and
- * reads nothing earlier work writes until that work has completed. */
+ * The step is one persistent launch per pass of at most 4 rows (m > 4 runs
+ * ceil(m / 4) passes): every CTA first rotates and quantises x into shared
+ * memory, then streams its tiles of gate/up; the CTA that completes a
+ * 128-block of h rotates and quantises it, and the down phase of each CTA
+ * starts on a segment of qh as soon as that segment is ready.  The launch uses
+ * programmatic stream serialisation, so it may start while earlier work in
+ * the stream drains, reading nothing earlier work writes until that work has
+ * completed. */
 tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
                       const uint16_t *x, int32_t m, float *y, void *workspace,
                       size_t workspace_bytes, tq_stream_t stream);
 
-/* The three kernels of tq_ffn_step as separate calls on the same workspace
+/* The three stages of tq_ffn_step as separate launches on the same workspace
  * (for timing a stage on its own): stage_input rotates and quantises x into
  * the workspace; stage_gateup runs gate/up + SiLU*up and the rotation of h;
  * stage_down writes y.  Issued in that order they compute tq_ffn_step. */
@@ -190,7 +194,7 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
  * and offers no allocator, or a real-time loop whose rules forbid calling the
  * allocator after start-up.  tq_ffn_step_static serves them: it computes
  * exactly what tq_ffn_step computes, with its scratch in a fixed array of
- * tq_ffn_static_workspace_bytes() bytes (about 1.1 MB) that is part of the
+ * tq_ffn_static_workspace_bytes() bytes (about 1.4 MB) that is part of the
  * library.  Every GPU that loads the library holds one such array until the
  * process exits.  The call allocates nothing (no cudaMalloc, no cudaFree).
  *
