@@ -33,8 +33,9 @@ constexpr size_t kWsAlign = 256;
 //   qx int8 [m][hidden] | sx f32 [m][hidden/128] | h bf16 [m][inter] |
 //   qh int8 [m][inter]  | sh f32 [m][inter/128]  | counters u32 [inter/128] |
 //   ybuf f32 [m][hidden] | err u32 (nonzero: a kernel's bounded wait ran out) |
-//   sync u32 [2 + inter/1024] (the step kernel's count of CTAs done and, per
-//   1024-wide segment of h, its rotated 128-blocks; zero between calls) |
+//   sync: u64 launch ticket, then u32 [inter/1024] per 1024-wide segment of h,
+//   its rotated 128-blocks (both count up over every step kernel launched on
+//   the workspace; tq_ffn_workspace_init zeroes them) |
 //   hst i8 [m*inter] (h quantised again, staged as the down phase reads it:
 //   per pass of rows r0.., [inter/128][rows][128] permuted) |
 //   hsn (f32 scale, i32 0x4b400000 - sum q) [m][inter/128]
@@ -69,7 +70,7 @@ struct FfnPtrs {
     unsigned *counters;
     float *ybuf;
     unsigned *err;
-    unsigned *done;
+    unsigned long long *ticket;
     unsigned *segready;
     uint8_t *hst;
     float2 *hsn;
@@ -81,7 +82,7 @@ FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
                    reinterpret_cast<uint16_t *>(b + L.h), reinterpret_cast<int8_t *>(b + L.qh),
                    reinterpret_cast<float *>(b + L.sh), reinterpret_cast<unsigned *>(b + L.counters),
                    reinterpret_cast<float *>(b + L.ybuf), reinterpret_cast<unsigned *>(b + L.err),
-                   reinterpret_cast<unsigned *>(b + L.sync), reinterpret_cast<unsigned *>(b + L.sync) + 1, b + L.hst,
+                   reinterpret_cast<unsigned long long *>(b + L.sync), reinterpret_cast<unsigned *>(b + L.sync) + 2, b + L.hst,
                    reinterpret_cast<float2 *>(b + L.hsn)};
 }
 
@@ -167,7 +168,7 @@ void set_ws_rows(tq::Call &c, const FfnPtrs &P, int r0, int hidden, int inter) {
     c.hst = P.hst + static_cast<size_t>(r0) * inter;
     c.hsn = P.hsn + static_cast<size_t>(r0) * (inter / 128);
     c.hcount = P.counters;
-    c.done = P.done;
+    c.ticket = P.ticket;
     c.segready = P.segready;
     c.err = P.err;
 }

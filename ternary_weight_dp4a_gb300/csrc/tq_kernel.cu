@@ -13,6 +13,7 @@ namespace tq {
 namespace {
 
 constexpr int kMaxDev = 64;
+constexpr int kPrologueSlots = 16;     // units in flight before the input is staged
 
 struct DevInfo {
     int sms = 0;
@@ -44,11 +45,45 @@ struct Plan {
     uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt;
     size_t bytes;
     int slots, grid, tiles_max, nseg_max;
+    Deal deal_a, deal_b;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// q or q + 1 tiles per CTA.
+Deal uniform_deal(int ntiles, int G) {
+    const int q = ntiles / G, r = ntiles % G;
+    return Deal{{q + 1, q, q, q}, {r, G, G}};
+}
+
+// Phase A's deal for a launch running both phases, phase B dealt uniformly
+// in reverse (the last ntB % G CTAs of phase A's order hold one more phase-B
+// tile).  Per CTA load = uA * (phase-A tiles) + uB * (phase-B tiles) units;
+// the deal takes the smallest bound L on every CTA's load that leaves room
+// for all ntA tiles, and gives the tiles beyond ntA back from the end of each
+// group, keeping the counts non-increasing in dealing order.
+Deal balanced_deal_a(int ntA, int uA, int ntB, int uB, int G) {
+    const int bq = ntB / G, rB = ntB % G;
+    const int nL = G - rB, nH = rB;
+    const long long total = static_cast<long long>(ntA) * uA + static_cast<long long>(ntB) * uB;
+    for (long long L = (total + G - 1) / G;; ++L) {
+        const long long A1 = std::max(0ll, (L - static_cast<long long>(bq) * uB) / uA);
+        const long long A2 = nH > 0 ? std::max(0ll, (L - static_cast<long long>(bq + 1) * uB) / uA) : A1;
+        const long long room = nL * A1 + nH * A2;
+        if (room < ntA) continue;
+        // each step of L adds at most G tiles of room, so the excess is below
+        // G unless the first bound tried already had room to spare
+        if (room - ntA >= G) return uniform_deal(ntA, G);
+        const int E = static_cast<int>(room - ntA);
+        const int a1 = static_cast<int>(A1), a2 = static_cast<int>(A2);
+        if (a1 == a2) return Deal{{a1, a1 - 1, a1 - 1, a1 - 1}, {G - E, G, G}};
+        const int e1 = std::min(E, nL), e2 = E - e1;
+        if (e2 > 0 && a2 == 0) return uniform_deal(ntA, G);
+        return Deal{{a1, a1 - 1, a2, a2 - 1}, {nL - e1, nL, G - e2}};
+    }
+}
 
 // Shared-memory plan: ring slots as many as fit (at most kMaxSlots), after
 // both phases' activations and (scale, magic - sum) pairs, the segment sums
@@ -63,15 +98,15 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     const int G = p->grid;
     const int nbA = kA / kBlock, nbB = kB / kBlock;
     const int uptA = 2 * ceil_div(nbA, kSegBlocks), uptB = ceil_div(nbB, kSegBlocks);
-    const int tpcA = c.do_a ? phase_tiles_max(nA, G) : 0, tpcB = c.do_b ? phase_tiles_max(nB, G) : 0;
-    // the epilogue warp tracks this CTA's phase-A tiles in a 32-bit mask
-    if (c.do_a && c.rotate_h && tpcA > 32) return false;
+    p->deal_b = uniform_deal(tilesB, G);
+    p->deal_a = c.do_a && c.do_b ? balanced_deal_a(tilesA, uptA, tilesB, uptB, G) : uniform_deal(tilesA, G);
+    const int tpcA = c.do_a ? p->deal_a.lv[0] : 0, tpcB = c.do_b ? p->deal_b.lv[0] : 0;
     p->tiles_max = std::max(1, std::max(tpcA, tpcB));
     p->nseg_max = std::max(1, uptB);
     const size_t actA = static_cast<size_t>(nbA) * kBlock * c.m, snA = static_cast<size_t>(nbA) * c.m * 8;
     const size_t actB = static_cast<size_t>(nbB) * kBlock * c.m, snB = static_cast<size_t>(nbB) * c.m * 8;
     const size_t part = static_cast<size_t>(tpcA * uptA + tpcB * uptB) * c.m * kTileRows * 4;
-    const size_t ints = static_cast<size_t>(3 * p->tiles_max + p->nseg_max) * 4;
+    const size_t ints = static_cast<size_t>(2 * p->tiles_max + p->nseg_max) * 4;
     // every region starts on a 128-byte boundary (the activations are read
     // and written 16 bytes at a time)
     constexpr size_t kAlign = 128;
@@ -79,8 +114,9 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
                          align_up(snB, kAlign) + align_up(part, kAlign) + align_up(ints, kAlign);
     const size_t budget = static_cast<size_t>(d.smem_optin) - 2048;   // static shared memory < 1 KB
     if (fixed >= budget) return false;
-    const int slots = static_cast<int>(std::min<size_t>(kMaxSlots, (budget - fixed) / (kCodesSlot + kScalesSlot)));
-    if (slots < 4) return false;
+    int slots = static_cast<int>(std::min<size_t>(kMaxSlots, (budget - fixed) / (kCodesSlot + kScalesSlot)));
+    slots -= slots % kProducerLanes;      // each slot filled by one producer lane
+    if (slots < 2 * kProducerLanes) return false;
     p->slots = slots;
     size_t off = static_cast<size_t>(slots) * kCodesSlot;
     p->off_scales = static_cast<uint32_t>(off);
@@ -192,7 +228,10 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     if (c.do_b && (e = make_mat(&a.mat[2], c.wb, c.fmt)) != cudaSuccess) return e;
     a.do_a = c.do_a;
     a.do_b = c.do_b;
+    a.deal_a = p.deal_a;
+    a.deal_b = p.deal_b;
     a.slots = p.slots;
+    a.prologue_slots = std::min(p.slots, kPrologueSlots);
     a.off_scales = p.off_scales;
     a.off_act = p.off_act;
     a.off_sn = p.off_sn;
@@ -224,7 +263,7 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.y = c.y;
     a.dots = c.dots;
     a.segready = c.segready;
-    a.done = c.done;
+    a.ticket = c.ticket;
     a.err = c.err;
     const bool coop = c.do_a && c.do_b;     // phase B waits on other CTAs' rotations
     if (c.fmt == TQ_FMT_TERNARY2) {

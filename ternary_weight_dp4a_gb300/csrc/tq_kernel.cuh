@@ -6,23 +6,22 @@
 // Work.  A phase multiplies m <= 4 activation rows by one or two weight
 // matrices of n rows x k.  Its unit of work is 16 weight rows x one segment
 // (8 consecutive 128-blocks) of one matrix: 4 KB of codes + 256 B of scales,
-// one ring slot.  A CTA owns whole 16-row tiles (dealt out strided, see
-// phase_geo); the units of its tiles go round-robin to its compute warps.  Each unit
+// one ring slot.  A CTA owns whole 16-row tiles (dealt in rounds, see Deal);
+// its compute warps claim the units of its tiles as they come free.  Each unit
 // yields the segment sums S_j (fold order: ascending blocks from +0) of its 16
 // outputs; the warp that completes a tile's last unit folds the S_j with the
 // pairwise tree and runs the tile's epilogue.
 //
 // Phase A (gate/up): input x rotated + quantised by every CTA (or read as
-// int8), units of gate and up, epilogue h = bf16(silu(g) * u); the CTA that
-// completes the last tile of a 128-block of h rotates and quantises it.
+// int8), units of gate and up, epilogue h = bf16(silu(g) * u); the CTA whose
+// tile completes a 128-block of h rotates and quantises that block.
 // Phase B (down, or a plain GEMV): input int8 rows staged from global memory,
 // epilogue y (fp32), optionally the int32 block dots.
 // A step runs A and B in one launch without a grid barrier: a phase-B unit
 // waits only until the 8 blocks of h its segment reads are rotated.  The
 // producer never waits for the consumers' phases: weights do not depend on
-// activations, so it streams the next phase's tiles (and, before
-// griddepcontrol.wait, this launch's first tiles while the previous launch
-// drains).
+// activations, so it streams the next phase's tiles (and this launch's first
+// few tiles while the previous launch drains and the input is staged).
 #pragma once
 
 #include <cuda.h>
@@ -40,7 +39,39 @@ constexpr int kCodesSlot = 4096;        // 16 rows x 8 blocks of codes (2-bit: t
 constexpr int kScalesSlot = 256;        // 16 rows x 8 fp16 scales
 constexpr int kMaxSlots = 48;
 constexpr int kMaxRowsPerPass = 4;
+// Producer lanes; lane l issues units k = l (mod kProducerLanes).  The ring
+// has a multiple of kProducerLanes slots, so every fill of a slot comes from
+// one lane, in order: when that lane waits for a slot's previous fill to be
+// released, every earlier release of the slot has happened, and the phase
+// parity it waits on cannot alias an older phase.
+constexpr int kProducerLanes = 4;
 constexpr int kTilesPerHBlock = kBlock / kTileRows;   // 16-row tiles per 128-block of h
+
+// How a phase's 16-row tiles are dealt to the CTAs.  CTA d (in dealing
+// order) takes lv[0] tiles if d < t[0], else lv[1] if d < t[1], else lv[2] if
+// d < t[2], else lv[3]; lv is non-increasing, so the CTAs that take more than
+// i tiles are a prefix of the dealing order for every i.  Tiles go out in
+// rounds: round i gives the next tile to each CTA of that prefix in turn, so
+// every round covers a contiguous range of tiles, and the blocks of h fill up
+// round after round over phase A.
+struct Deal {
+    int lv[4];
+    int t[3];
+};
+
+__host__ __device__ inline int deal_count(const Deal &d, int c) {
+    return c < d.t[0] ? d.lv[0] : c < d.t[1] ? d.lv[1] : c < d.t[2] ? d.lv[2] : d.lv[3];
+}
+
+// Tile of the j-th local tile of CTA c: the tiles of rounds 0..j-1, plus c.
+__host__ __device__ inline int deal_tile(const Deal &d, int G, int c, int j) {
+    // rounds [0, lv[3]) serve G CTAs, [lv[3], lv[2]) t[2], [lv[2], lv[1]) t[1], [lv[1], lv[0]) t[0]
+    int base = min(j, d.lv[3]) * G;
+    base += max(0, min(j, d.lv[2]) - d.lv[3]) * d.t[2];
+    base += max(0, min(j, d.lv[1]) - d.lv[2]) * d.t[1];
+    base += max(0, min(j, d.lv[0]) - d.lv[1]) * d.t[0];
+    return base + c;
+}
 
 struct MatDesc {
     CUtensorMap tm_codes;     // uint8 {row bytes, n}, box {128, 16}, 128-byte swizzle; or
@@ -56,7 +87,9 @@ enum : int { kInRotX = 0, kInNormY = 1, kInPlain = 2 };
 struct KArgs {
     MatDesc mat[3];           // phase A: gate, up; phase B: mat[2]
     int do_a, do_b;
+    Deal deal_a, deal_b;      // tiles per CTA of each phase
     int slots;                // ring slots
+    int prologue_slots;       // units the producer issues before the input is staged
     // dynamic shared memory: ring codes | ring scales | phase A activation +
     // (scale, magic - sum) pairs | phase B activation + pairs | segment sums |
     // int counters: units per tile, tiles folded, phase B segment state
@@ -78,7 +111,7 @@ struct KArgs {
     float *sh;
     uint8_t *hst;             // h staged for phase B: [inter/128][M][128] int8
     float2 *hsn;              // [inter/128][M] (scale, magic - sum q as int bits)
-    unsigned *hcount;         // [inter/128]; zero on entry and on exit
+    unsigned *hcount;         // rows of each 128-block of h published; zero on entry and on exit
     // phase B input: staged (bst/bsn, as phase A's rotation writes them) or
     // plain int8 qb [M][kB] + fp32 sb [M][kB/128]
     const uint8_t *bst;
@@ -87,23 +120,29 @@ struct KArgs {
     const float *sb;
     float *y;                 // fp32 [M][nB]
     int32_t *dots;            // int32 [M][nB][kB/128] or null
-    unsigned *segready;       // per 8-block segment of h: its 128-blocks rotated (A+B launches)
-    unsigned *done;           // CTAs finished with phase B (A+B launches); zero on entry and exit
-    unsigned *err;            // bit 0: producer wait, 1: producer drain, 2: consumer wait, 4: grid barrier
+    // A+B launches: per 8-block segment of h, the count of its 128-blocks
+    // rotated, over every launch on this workspace (never reset: launch e
+    // waits for (e + 1) x blocks); the launch ticket gives e: every CTA takes
+    // one ticket per launch, so launch e's CTAs hold tickets [e G, (e + 1) G)
+    unsigned *segready;
+    unsigned long long *ticket;
+    unsigned *err;            // wait that ran out: bit 0 producer (slot free), 1 producer drain,
+                              // 2 consumer (slot data), 3 consumer (slot issued), 4 producer
+                              // (input staged), 5 epilogue (tile folded), 6 phase B (segment of h)
 };
 
-// The tiles and units of one phase for CTA c of G.  Tiles are dealt out
-// strided: CTA c takes tiles start, start + G, ... with start = c (phase A)
-// or G - 1 - c (phase B), so the CTAs holding one more phase-A tile are not
-// the ones holding one more phase-B tile, and the 128-blocks of h complete
-// evenly over phase A.  Unit order: phase A tile-major (tile, matrix,
-// segment); phase B segment-major (segment, tile), so that a CTA needs the
-// segments of h in the order they become ready.
+// The tiles and units of one phase for CTA c of G.  Phase A deals in CTA
+// order, phase B in reverse (dealing index G - 1 - c), so the CTAs holding
+// one more phase-B tile are the ones the host gave fewer phase-A tiles.  Unit
+// order: phase A tile-major (tile, matrix, segment); phase B segment-major
+// (segment, tile), so that a CTA needs the segments of h in the order they
+// become ready.
 struct PhaseGeo {
-    int n, k, nb, nseg, upt, ntiles, start, count, units;
+    int n, k, nb, nseg, upt, ntiles, dc, count, units;
+    Deal deal;
 };
 
-__host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int c, bool reverse) {
+__host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int c, bool reverse, const Deal &d) {
     PhaseGeo p{};
     if (n <= 0) return p;
     p.n = n;
@@ -112,21 +151,28 @@ __host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int
     p.nseg = (p.nb + kSegBlocks - 1) / kSegBlocks;
     p.upt = nmat * p.nseg;
     p.ntiles = (n + kTileRows - 1) / kTileRows;
-    p.start = reverse ? G - 1 - c : c;
-    p.count = p.start < p.ntiles ? (p.ntiles - 1 - p.start) / G + 1 : 0;
+    p.dc = reverse ? G - 1 - c : c;
+    p.deal = d;
+    p.count = deal_count(d, p.dc);
     p.units = p.count * p.upt;
     return p;
 }
 
-// Largest tile count phase_geo gives any CTA.
-__host__ __device__ inline int phase_tiles_max(int n, int G) {
-    const int ntiles = (n + kTileRows - 1) / kTileRows;
-    return (ntiles + G - 1) / G;
-}
+__device__ __forceinline__ int phase_tile(const PhaseGeo &p, int G, int lt) { return deal_tile(p.deal, G, p.dc, lt); }
 
 // Fire-and-forget add at gpu scope (nothing waits for a returned value).
 __device__ __forceinline__ void red_add_relaxed_gpu(unsigned *p, unsigned v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Release/acquire fence at gpu scope (cumulative: orders what this thread
+// has observed, e.g. its warp's stores before a __syncwarp).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
@@ -343,21 +389,30 @@ __device__ __forceinline__ void stage_plain_range(const int8_t *__restrict__ q, 
 // GPU); other warps wait for it.  Returns false if a bounded wait ran out.
 template <int FMT, int M>
 __device__ bool stage_segment_b(const KArgs &a, const PhaseGeo &P, int j, uint8_t *act_h, float2 *sn_h,
-                                int *segst, int lane) {
+                                int *segst, unsigned epoch, int lane) {
     volatile int *vst = segst;
-    if (vst[j] == 2) {
+    // lane 0 reads the segment's state and claims it; the warp follows its
+    // broadcast (per-lane reads of a flag can differ and split the warp)
+    int state = 0;
+    if (lane == 0) {
+        state = vst[j];
+        if (state != 2) state = atomicCAS(&segst[j], 0, 1) == 0 ? 3 : 1;
+    }
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state == 2) {
         __threadfence_block();
         return true;
     }
-    int claim = 0;
-    if (lane == 0) claim = atomicCAS(&segst[j], 0, 1) == 0;
-    claim = __shfl_sync(0xffffffffu, claim, 0);
+    const int claim = state == 3;
     const int b0 = j * kSegBlocks, bc = min(kSegBlocks, P.nb - b0);
     int ok = 1;
     if (claim) {
         if (a.do_a && lane == 0) {
             const long long t0 = clock64();
-            while (ld_acquire_u32(a.segready + j) < static_cast<unsigned>(bc)) {
+            // counts wrap modulo 2^32; this launch's target is never more
+            // than bc ahead of the count
+            const unsigned target = (epoch + 1u) * static_cast<unsigned>(bc);
+            while (static_cast<int>(ld_acquire_u32(a.segready + j) - target) < 0) {
                 if (clock64() - t0 > kWaitBudgetCycles) {
                     ok = 0;
                     break;
@@ -406,12 +461,134 @@ __device__ __forceinline__ void unit_advance(UnitPos &u, int step, int extent) {
     }
 }
 
+// Element of a block at staged position p (the inverse of staged_pos).
+template <int FMT>
+__device__ __forceinline__ int staged_elem(int p) {
+    if (FMT == 0) {
+        const int q = p & 15, g = q >> 2;
+        return (p & ~15) + (((g & 1) << 3) | ((q & 3) << 1) | (g >> 1));
+    }
+    return (p & ~31) + 8 * (p & 3) + ((p >> 2) & 7);
+}
+
+// One butterfly stage of the 128-point transform on values held in staged
+// order (lane l holds staged positions 4l..4l+3 in v[0..3]).  The stage's
+// element span maps to a lane bit (xor mask lm) or to a bit of the register
+// index (rm); the element with the bit clear keeps a + b, the other a - b.
+__device__ __forceinline__ void wht_stage(float (&v)[4], int lane, int lm, int rm) {
+    if (lm != 0) {
+        const bool upper = (lane & lm) != 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[c], lm);
+            v[c] = upper ? __fsub_rn(other, v[c]) : __fadd_rn(v[c], other);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if ((c & rm) == 0) {
+                const float x = v[c], y = v[c | rm];
+                v[c] = __fadd_rn(x, y);
+                v[c | rm] = __fsub_rn(x, y);
+            }
+    }
+}
+
+// Rotate and quantise 128-block hb of h (all M rows, every row of it
+// published).  The transform runs in the staged order phase B reads: the
+// stages go in element-span order 1, 2, ..., 64, each elementwise, so the
+// values are those of the natural-order transform, and each lane's four codes
+// are four consecutive staged bytes (one store).  The staged copy hst/hsn is
+// written first and released (fence, then the block's add to its segment's
+// ready counter when phase B runs in this launch); qh/sh for the caller and
+// the block's count reset come after.
+template <int FMT, int M>
+__device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, int lane) {
+    const int nbh = n / kBlock;
+    float v[M][4];
+    if (FMT == 0) {
+        // staged positions 4l..4l+3 hold elements b, b+2, b+4, b+6 of the
+        // 16-group l/4, b in {0, 8, 1, 9}: the low or high halves of one
+        // aligned 16-byte word of h
+        const int g = lane & 3, b = ((g & 1) << 3) | (g >> 1);
+#pragma unroll
+        for (int rr = 0; rr < M; ++rr) {
+            const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(a.h + static_cast<size_t>(rr) * n + hb * kBlock +
+                                                                   (lane >> 2) * 16 + (b & 8)));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                v[rr][c] = bf16_bits_to_f32(static_cast<uint16_t>((b & 1) ? (ws[c] >> 16) : (ws[c] & 0xffffu)));
+        }
+    } else {
+#pragma unroll
+        for (int rr = 0; rr < M; ++rr)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                v[rr][c] = bf16_bits_to_f32(__ldcg(a.h + static_cast<size_t>(rr) * n + hb * kBlock + staged_elem<FMT>(4 * lane + c)));
+    }
+    // element span 1, 2, ..., 64 -> (lane xor mask, register bit)
+    constexpr int kLm[2][7] = {{2, 0, 0, 1, 4, 8, 16}, {1, 2, 4, 0, 0, 8, 16}};
+    constexpr int kRm[2][7] = {{0, 1, 2, 0, 0, 0, 0}, {0, 0, 0, 1, 2, 0, 0}};
+    const float cs = __uint_as_float(0x3db504f3u);  // (float)(1/sqrt(128))
+    int8_t q[M][4];
+    float sc[M];
+#pragma unroll
+    for (int rr = 0; rr < M; ++rr) {
+#pragma unroll
+        for (int st = 0; st < 7; ++st) wht_stage(v[rr], lane, kLm[FMT][st], kRm[FMT][st]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[rr][c] = __fmul_rn(v[rr][c], cs);
+        // absmax over the block: the order of non-negative floats is that of their bits
+        const float lmax = fmaxf(fmaxf(fabsf(v[rr][0]), fabsf(v[rr][1])), fmaxf(fabsf(v[rr][2]), fabsf(v[rr][3])));
+        const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(lmax)));
+        sc[rr] = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
+        int sum = 0;
+        uint32_t word = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            int t = 0;
+            if (amax != 0.0f) {
+                t = __float2int_rn(__fdiv_rn(v[rr][c], sc[rr]));
+                t = t > 127 ? 127 : (t < -127 ? -127 : t);
+            }
+            q[rr][c] = static_cast<int8_t>(t);
+            sum += t;
+            word |= (static_cast<uint32_t>(t) & 0xffu) << (8 * c);
+        }
+        sum = __reduce_add_sync(0xffffffffu, sum);
+        *reinterpret_cast<uint32_t *>(a.hst + static_cast<size_t>(hb * M + rr) * kBlock + 4 * lane) = word;
+        if (lane == 0) a.hsn[hb * M + rr] = block_sn(sc[rr], sum);
+    }
+    __syncwarp();
+    if (lane == 0 && a.do_b) {
+        fence_acq_rel_gpu();
+        red_add_relaxed_gpu(a.segready + hb / kSegBlocks, 1u);
+    }
+#pragma unroll
+    for (int rr = 0; rr < M; ++rr) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            a.qh[static_cast<size_t>(rr) * n + hb * kBlock + staged_elem<FMT>(4 * lane + c)] = q[rr][c];
+        if (lane == 0) a.sh[static_cast<size_t>(rr) * nbh + hb] = sc[rr];
+    }
+    if (lane == 0) a.hcount[hb] = 0u;
+}
+
 template <int FMT, int M>
 __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxSlots];
     __shared__ __align__(8) uint64_t empty_bar[kMaxSlots];
+    __shared__ __align__(8) uint64_t input_bar;     // phase A's input staged (one arrival)
     __shared__ float s_warp[8];
+    __shared__ int s_next;                           // next unit a compute warp claims
+    __shared__ unsigned s_epoch;                     // this launch's index on the workspace (A+B launches)
+    // unit the producer last issued into each slot.  A consumer waits for its
+    // unit's number here before it waits for the slot's data: a warp may
+    // claim unit k + S while unit k still waits for its data, and the slot's
+    // barrier phase parity alone cannot tell those two fills apart.
+    __shared__ int slot_unit[kMaxSlots];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -424,14 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     uint8_t *act_h = base + a.off_acth;
     float2 *sn_h = reinterpret_cast<float2 *>(base + a.off_snh);
     float *part = reinterpret_cast<float *>(base + a.off_part);
-    // int counters: units done per local tile of phase A, of phase B; phase A
-    // tiles folded; phase B segments (0 absent, 1 staging, 2 staged)
+    // int counters: units done per local tile of phase A, of phase B; phase B
+    // segments (0 absent, 1 staging, 2 staged)
     int *tcnt = reinterpret_cast<int *>(base + a.off_tcnt);
-    int *tdone = tcnt + 2 * a.tiles_max;
-    int *segst = tdone + a.tiles_max;
+    int *segst = tcnt + 2 * a.tiles_max;
 
-    const PhaseGeo ga = a.do_a ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta, false) : PhaseGeo{};
-    const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta, true) : PhaseGeo{};
+    const PhaseGeo ga = a.do_a ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta, false, a.deal_a) : PhaseGeo{};
+    const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta, true, a.deal_b) : PhaseGeo{};
     const int total = ga.units + gb.units;
 
     if (threadIdx.x == 0) {
@@ -439,9 +615,12 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
+        mbar_init(smem_u32(&input_bar), 1);
         mbar_init_fence();
+        s_next = 0;
     }
-    for (int i = threadIdx.x; i < 3 * a.tiles_max + a.nseg_max; i += kThreads) tcnt[i] = 0;
+    for (int i = threadIdx.x; i < kMaxSlots; i += kThreads) slot_unit[i] = -1;
+    for (int i = threadIdx.x; i < 2 * a.tiles_max + a.nseg_max; i += kThreads) tcnt[i] = 0;
     __syncthreads();
     pdl_launch_dependents();
 
@@ -449,10 +628,13 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
         // ------------------------------------------------------------ producer
         // Lanes 0..kProducerLanes-1 each issue every kProducerLanes-th unit,
         // so several units are in the issue pipe at once; unit positions and
-        // (slot, round) = divmod(k, S) advance incrementally.
-        constexpr int kProducerLanes = 4;
+        // (slot, round) = divmod(k, S) advance incrementally.  Only the first
+        // prologue_slots units go out before the consumers have staged the
+        // input: the input's loads would otherwise queue behind a full ring
+        // of weight copies.
         if (lane < kProducerLanes) {
             bool ok = true;
+            unsigned bad = 0u;
             int k = lane;
             bool in_a = k < ga.units;
             UnitPos u{0, in_a ? k : k - ga.units};
@@ -475,9 +657,18 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                     lt = u.inner;
                     mi = 2;
                 }
-                const int tile = P.start + lt * G;
+                const int tile = phase_tile(P, G, lt);
                 const MatDesc &md = a.mat[mi];
-                if (round > 0 && !(ok = mbar_wait(smem_u32(&empty_bar[slot]), (round - 1) & 1))) break;
+                if (k >= a.prologue_slots && k < a.prologue_slots + kProducerLanes &&
+                    !(ok = mbar_wait(smem_u32(&input_bar), 0))) {
+                    bad |= 16u;
+                    break;
+                }
+                if (round > 0 && !(ok = mbar_wait(smem_u32(&empty_bar[slot]), (round - 1) & 1))) {
+                    bad |= 1u;
+                    break;
+                }
+                reinterpret_cast<volatile int *>(slot_unit)[slot] = k;
                 const uint32_t fb = smem_u32(&full_bar[slot]);
                 const uint32_t dst = smem_u32(codes_ring + static_cast<size_t>(slot) * kCodesSlot);
                 const bool sct = md.scales_tma != 0;
@@ -501,20 +692,18 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                     ++round;
                 }
             }
-            if (!ok && a.err != nullptr) atomicOr(a.err, 1u);
-        }
-        __syncwarp();
-        if (lane == 0) {
-            // no copy may still be landing in shared memory when the CTA exits
-            const int k0 = total > S ? total - S : 0;
-            int slot = k0 % S, round = k0 / S;
-            for (int k = k0; k < total; ++k) {
-                if (!mbar_wait(smem_u32(&full_bar[slot]), round & 1) && a.err != nullptr) atomicOr(a.err, 2u);
-                if (++slot == S) {
-                    slot = 0;
-                    ++round;
+            // no copy may still be landing in shared memory when the CTA
+            // exits.  Every fill of a slot comes from one lane, so this lane's
+            // last S / kProducerLanes units are the last fills of its slots
+            // (earlier fills were consumed before their slot was refilled):
+            // wait for those, newest first.  When the consumers took every
+            // unit, all have landed and each check returns at once.
+            for (int kk = k - kProducerLanes, n = 0; kk >= 0 && n < S / kProducerLanes; kk -= kProducerLanes, ++n)
+                if (!mbar_wait(smem_u32(&full_bar[kk % S]), (kk / S) & 1)) {
+                    bad |= 2u;
+                    break;
                 }
-            }
+            if (bad != 0u && a.err != nullptr) atomicOr(a.err, bad);
         }
         return;
     }
@@ -522,7 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     // -------------------------------------------------------------- consumers
     const int tid = threadIdx.x;             // 0 .. kConsumers-1
     bool ok = true;
+    unsigned bad = 0u;                       // error bits of the waits that ran out
     pdl_wait();
+    // A+B launches that rotate h take a launch ticket; its result is needed
+    // only in phase B, so it is stored after the input is staged
+    const bool ticketed = a.do_a && a.do_b && a.rotate_h;
+    unsigned long long ticket = 0;
+    if (ticketed && tid == 0) ticket = atomicAdd(a.ticket, 1ull);
 
     // ---- phase A's activation: every CTA rotates + quantises the input
     if (a.do_a) {
@@ -559,30 +754,47 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
         } else {
             stage_plain_range<FMT, M>(a.qa, a.sa, hidden, 0, ga.nb, act_x, sn_x, warp, kConsumerWarps, lane);
         }
+        if (ticketed && tid == 0) s_epoch = static_cast<unsigned>(ticket / static_cast<unsigned long long>(G));
         named_barrier(1, kConsumers);
     }
+    if (tid == 0) mbar_arrive(smem_u32(&input_bar));
 
-    // ---- units: CTA-local index k over phase A then phase B, compute warp
-    // k % ncw.  A compute warp waits only for its data (and, in phase B, for
-    // the segment of h it needs); h-block bookkeeping runs on the epilogue
-    // warp, which computes units too when there is none.
-    const bool epi = a.do_a && a.rotate_h;
+    // ---- units: CTA-local index k over phase A then phase B.  A compute
+    // warp claims the next unit from a shared counter when it is free, so a
+    // warp that runs slow (or waits for a segment of h) holds up no other
+    // warp's units.  A warp's claims increase, so its unit positions and
+    // (slot, round) = divmod(k, S) advance incrementally.  When phase A
+    // rotates h, block hb is rotated by its owner, CTA G - 1 - (hb mod G)
+    // (owners spread one block per CTA as far as the blocks go), on its last
+    // consumer warp; a CTA that owns no block computes units on that warp too.
+    const int nbh = a.do_a ? ga.n / kBlock : 0;
+    const bool epi = a.do_a && a.rotate_h && G - 1 - cta < nbh;
     const int ncw = epi ? kComputeWarps : kConsumerWarps;
     int *tcnt_a = tcnt, *tcnt_b = tcnt + a.tiles_max;
     float *part_a = part, *part_b = part + static_cast<size_t>(ga.units) * M * kTileRows;
     if (warp < ncw) {
-        int k = warp;
-        bool in_a = k < ga.units;
-        UnitPos u{0, in_a ? k : k - ga.units};
-        unit_advance(u, 0, in_a ? max(ga.upt, 1) : max(gb.count, 1));
-        int slot = k % S, round = k / S;
+        int kp = 0, slot = 0, round = 0;
+        bool in_a = ga.units > 0;
+        UnitPos u{0, 0};
         int staged_seg = -1;
-        for (; k < total; k += ncw) {
+        for (;;) {
+            int k = 0;
+            if (lane == 0) k = atomicAdd(&s_next, 1);
+            k = __shfl_sync(0xffffffffu, k, 0);
+            if (k >= total) break;
             if (in_a && k >= ga.units) {
                 in_a = false;
-                u = UnitPos{0, k - ga.units};
-                unit_advance(u, 0, gb.count);
+                u = UnitPos{0, 0};
+                unit_advance(u, k - ga.units, gb.count);
+            } else {
+                unit_advance(u, k - kp, in_a ? ga.upt : gb.count);
             }
+            slot += k - kp;
+            while (slot >= S) {
+                slot -= S;
+                ++round;
+            }
+            kp = k;
             const PhaseGeo &P = in_a ? ga : gb;
             int mi, seg, lt;
             if (in_a) {
@@ -594,14 +806,33 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 lt = u.inner;
                 mi = 2;
                 if (seg != staged_seg) {
-                    if (!stage_segment_b<FMT, M>(a, P, seg, act_h, sn_h, segst, lane)) ok = false;
+                    if (!stage_segment_b<FMT, M>(a, P, seg, act_h, sn_h, segst, s_epoch, lane)) {
+                        ok = false;
+                        bad |= 64u;
+                    }
                     staged_seg = seg;
                 }
             }
             const int i = in_a ? k : k - ga.units;          // unit index within its phase
-            if (ok && !mbar_wait(smem_u32(&full_bar[slot]), round & 1)) ok = false;
+            if (ok && lane == 0) {
+                const volatile int *vsu = slot_unit;
+                const long long t0 = clock64();
+                while (vsu[slot] != k) {
+                    if (clock64() - t0 > kWaitBudgetCycles) {
+                        ok = false;
+                        bad |= 8u;
+                        break;
+                    }
+                    __nanosleep(20);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[slot]), round & 1))) {
+                ok = false;
+                bad |= 4u;
+            }
             if (!ok) break;
-            const int tile = P.start + lt * G;
+            const int tile = phase_tile(P, G, lt);
             const MatDesc &md = a.mat[mi];
             const uint8_t *cs = codes_ring + static_cast<size_t>(slot) * kCodesSlot;
             const int bcount = min(kSegBlocks, P.nb - seg * kSegBlocks);
@@ -632,12 +863,6 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             // the slot's codes and scales are all in registers: hand it back
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-            unit_advance(u, ncw, in_a ? P.upt : P.count);
-            slot += ncw;
-            while (slot >= S) {
-                slot -= S;
-                ++round;
-            }
 
             // segment sums of this unit -> shared memory; count the tile
             float *pu = (in_a ? part_a : part_b) + static_cast<size_t>(i) * M * kTileRows;
@@ -655,8 +880,8 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             __threadfence_block();
 
             // ---- the tile's last unit: fold its segment sums with the pairwise
-            // tree and store h (phase A) or y (phase B); no global fence here.
-            // Phase A units of a tile are consecutive; phase B's are `count` apart.
+            // tree and store h (phase A) or y (phase B).  Phase A units of a
+            // tile are consecutive; phase B's are `count` apart.
             const int r = lane >> 4;            // activation rows r, r + 2, ... of the tile's 16 outputs
             const size_t ustride = static_cast<size_t>(in_a ? 1 : P.count) * M * kTileRows;
             float *pt = (in_a ? part_a + static_cast<size_t>(lt) * P.upt * M * kTileRows : part_b + static_cast<size_t>(lt) * M * kTileRows) +
@@ -673,131 +898,45 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                     if (row < P.n) a.y[static_cast<size_t>(ra) * P.n + row] = yv;
                 }
             }
-            if (in_a && epi) {
+            if (in_a && a.rotate_h) {
+                // publish the tile's rows of h: a gpu-scope fence (cumulative
+                // over the warp's stores), then a fire-and-forget add of its
+                // rows to the block's count.  Only this warp waits for the
+                // fence; the others keep claiming units.
                 __syncwarp();
                 if (lane == 0) {
-                    __threadfence_block();
-                    atomicExch(&tdone[lt], 1);
+                    fence_acq_rel_gpu();
+                    red_add_relaxed_gpu(&a.hcount[tile / kTilesPerHBlock],
+                                        static_cast<unsigned>(min(kTileRows, P.n - tile * kTileRows)));
                 }
             }
         }
     } else if (epi) {
-        // ---- epilogue warp: publish each folded phase-A tile into its
-        // 128-block of h with a gpu-scope fence and a fire-and-forget add of
-        // its rows.  The CTA holding a block's last tile owns the block: after
-        // publishing that tile it waits for the block's 128 rows, rotates and
-        // quantises it, and (when this launch runs phase B) counts it into its
-        // segment's ready counter.
-        // Tiles are published in batches (every tile folded so far, behind one
-        // fence, one add per tile); an owned block is rotated as soon as its
-        // 128 rows are in, checked without blocking so that a late CTA never
-        // holds up this CTA's own publishing.  pend: owned tiles (bit lt)
-        // whose block still waits.
-        const volatile int *vd = tdone;
-        int lt = 0;
-        unsigned pend = 0u;
-        const long long w0 = clock64();
-        while ((lt < ga.count || pend != 0u) && ok) {
-            bool progress = false;
-            if (lt < ga.count && vd[lt] != 0) {
-                int lt_end = lt + 1;
-                while (lt_end < ga.count && lt_end - lt < 32 && vd[lt_end] != 0) ++lt_end;
-                __syncwarp();
-                __threadfence();
-                if (lane < lt_end - lt) {
-                    const int tile = ga.start + (lt + lane) * G;
-                    red_add_relaxed_gpu(&a.hcount[tile / kTilesPerHBlock],
-                                        static_cast<unsigned>(min(kTileRows, ga.n - tile * kTileRows)));
-                }
-                for (; lt < lt_end; ++lt) {
-                    const int tile = ga.start + lt * G;
-                    const int hb = tile / kTilesPerHBlock;
-                    if (tile == min((hb + 1) * kTilesPerHBlock, ga.ntiles) - 1) pend |= 1u << lt;
-                }
-                progress = true;
-            }
-            int own = -1;
-            if (pend != 0u) {
-                // the first pending owned block whose rows are all in, if any
-                int found = -1;
-                if (lane == 0) {
-                    for (unsigned m = pend; m != 0u; m &= m - 1u) {
-                        const int l = __ffs(m) - 1;
-                        const int hb = (ga.start + l * G) / kTilesPerHBlock;
-                        if (ld_acquire_u32(&a.hcount[hb]) == static_cast<unsigned>(kBlock)) {
-                            found = l;
-                            break;
-                        }
-                    }
-                }
-                own = __shfl_sync(0xffffffffu, found, 0);
-            }
-            if (own < 0) {
-                if (!progress) {
-                    if (clock64() - w0 > kWaitBudgetCycles) ok = false;
-                    __nanosleep(32);
-                }
-                continue;
-            }
-            pend &= ~(1u << own);
-            const int hb = (ga.start + own * G) / kTilesPerHBlock;
-            const int nbh = ga.n / kBlock;
-            float v[M][4];
-#pragma unroll
-            for (int rr = 0; rr < M; ++rr)
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    v[rr][cc] = bf16_bits_to_f32(__ldcg(a.h + static_cast<size_t>(rr) * ga.n + hb * kBlock + lane + 32 * cc));
-#pragma unroll
-            for (int rr = 0; rr < M; ++rr) wht128_warp(v[rr], lane);
-#pragma unroll
-            for (int rr = 0; rr < M; ++rr) {
-                int8_t q[4];
-                const float sc = quant_block_warp(v[rr], q);
-                int sum = 0;
-                uint8_t *hst = a.hst + static_cast<size_t>(hb * M + rr) * kBlock;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int e = lane + 32 * cc;
-                    a.qh[static_cast<size_t>(rr) * ga.n + hb * kBlock + e] = q[cc];
-                    hst[staged_pos<FMT>(e)] = static_cast<uint8_t>(q[cc]);
-                    sum += q[cc];
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                if (lane == 0) {
-                    a.sh[static_cast<size_t>(rr) * nbh + hb] = sc;
-                    a.hsn[hb * M + rr] = block_sn(sc, sum);
-                }
-            }
-            __syncwarp();
+        // ---- owner warp: rotate each owned block of h once all its rows are
+        // published.  Lane 0 polls the block's count; the warp follows its
+        // broadcast.
+        for (int own = G - 1 - cta; own < nbh; own += G) {
+            int ready = 0;
             if (lane == 0) {
-                a.hcount[hb] = 0u;
-                if (a.do_b) {
-                    __threadfence();
-                    red_add_relaxed_gpu(a.segready + hb / kSegBlocks, 1u);
+                const long long t0 = clock64();
+                while (!(ready = ld_relaxed_u32(&a.hcount[own]) == static_cast<unsigned>(kBlock))) {
+                    if (clock64() - t0 > kWaitBudgetCycles) break;
+                    __nanosleep(64);
                 }
+                // acquire: what the rows' publishers released is visible to
+                // lane 0, and through the warp's shuffle to every lane
+                fence_acq_rel_gpu();
             }
+            if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                ok = false;
+                bad |= 32u;
+                break;
+            }
+            rotate_h_block<FMT, M>(a, ga.n, own, lane);
         }
     }
 
-    // ---- a launch running both phases: the last CTA to finish resets the
-    // segment ready counters (no CTA reads them any more)
-    if (a.do_a && a.do_b && a.rotate_h) {
-        named_barrier(1, kConsumers);
-        if (warp == 0) {
-            if (lane == 0) {
-                __threadfence();
-                if (atomicAdd(a.done, 1u) == static_cast<unsigned>(G - 1)) {
-                    for (int j = 0; j < gb.nseg; ++j) a.segready[j] = 0u;
-                    *a.done = 0u;
-                    __threadfence();
-                }
-            }
-            __syncwarp();
-        }
-    }
-    if (!ok && lane == 0 && a.err != nullptr) atomicOr(a.err, 4u);
+    if (bad != 0u && lane == 0 && a.err != nullptr) atomicOr(a.err, bad);
 }
 
 }  // namespace tq

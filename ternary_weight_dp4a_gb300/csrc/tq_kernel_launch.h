@@ -43,7 +43,7 @@ struct Call {
     float *y;
     int32_t *dots;
     unsigned *segready;                 // per segment of h: rotated 128-blocks (A+B launches)
-    unsigned *done;
+    unsigned long long *ticket;         // launch tickets (A+B launches)
     unsigned *err;
 };
 

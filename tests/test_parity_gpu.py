@@ -189,9 +189,9 @@ def test_ffn_full_size_layer_and_packed_rows(tq, orc, fmt):
 
 
 def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
-    """The per-block completion counters are zero after every step, and the three
-    stage calls (the three-kernel path) compute exactly the step (the fused
-    single-kernel path at m <= 2)."""
+    """The per-block completion counters are zero after every step, the launch
+    ticket and the segment ready counters count exactly one launch, and the
+    three stage calls compute exactly the one-launch step."""
     import torch
     hidden, inter, m = 1024, 3072, 2
     mats = ffn_mats(hidden, inter, 0)
@@ -202,9 +202,13 @@ def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
     cnt = wsn[o["counters"]:o["counters"] + 4 * (inter // 128)].view(np.uint32)
     assert np.all(cnt == 0)
     assert wsn[o["err"]:o["err"] + 4].view(np.uint32)[0] == 0     # no wait ran out
-    # the CTA-done count and the per-segment ready counters return to zero
-    nsync = 2 + (inter + 1023) // 1024
-    assert np.all(wsn[o["sync"]:o["sync"] + 4 * nsync].view(np.uint32) == 0)
+    # one launch: one ticket per CTA (one CTA per SM), and every segment's
+    # ready counter counted each of its 128-blocks once
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert int(wsn[o["sync"]:o["sync"] + 8].view(np.uint64)[0]) == sms
+    nseg = (inter + 1023) // 1024
+    seg = wsn[o["sync"] + 8:o["sync"] + 8 + 4 * nseg].view(np.uint32)
+    assert list(seg) == [min(8, inter // 128 - 8 * j) for j in range(nseg)]
     g, u, d = mats
     ws2 = tq.ffn_workspace(m, hidden, inter)
     y2 = torch.empty((m, hidden), dtype=torch.float32, device="cuda")
