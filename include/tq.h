@@ -149,10 +149,13 @@ tq_status tq_ffn_workspace_init(void *workspace, size_t workspace_bytes, tq_stre
  * x: bf16 bits [m][hidden], 16-byte aligned.  y: fp32 [m][hidden].
  * workspace: >= tq_ffn_workspace_bytes(m, hidden, inter) bytes, 256-byte
  * aligned, initialised once by tq_ffn_workspace_init; it holds the step's
- * intermediates (qx, sx, h, qh, sh, the per-block partial dots of h) and the
- * per-block and per-segment completion counters of h, which every call leaves
- * at zero.  Calls sharing a workspace must not run
- * concurrently.
+ * intermediates (qx, sx, h, qh, sh, h quantised again in the layout the down
+ * phase reads) and the step's synchronisation state: per 128-block of h a
+ * count of published rows (every call leaves it at zero), a launch ticket
+ * and per 1024-wide segment of h a count of rotated blocks (both count up
+ * over the calls on the workspace; a launch derives its index from its
+ * ticket).  After a call that failed in flight the workspace must be
+ * initialised again.  Calls sharing a workspace must not run concurrently.
  * The step is one persistent launch per pass of at most 4 rows (m > 4 runs
  * ceil(m / 4) passes): every CTA first rotates and quantises x into shared
  * memory, then streams its tiles of gate/up; the CTA that completes a
