@@ -197,7 +197,7 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
  * and offers no allocator, or a real-time loop whose rules forbid calling the
  * allocator after start-up.  tq_ffn_step_static serves them: it computes
  * exactly what tq_ffn_step computes, with its scratch in a fixed array of
- * tq_ffn_static_workspace_bytes() bytes (about 1.4 MB) that is part of the
+ * tq_ffn_static_workspace_bytes() bytes (about 2.5 MB) that is part of the
  * library.  Every GPU that loads the library holds one such array until the
  * process exits.  The call allocates nothing (no cudaMalloc, no cudaFree).
  *

@@ -38,9 +38,11 @@ constexpr size_t kWsAlign = 256;
 //   the workspace; tq_ffn_workspace_init zeroes them) |
 //   hst i8 [m*inter] (h quantised again, staged as the down phase reads it:
 //   per pass of rows r0.., [inter/128][rows][128] permuted) |
-//   hsn (f32 scale, i32 0x4b400000 - sum q) [m][inter/128]
+//   hsn (f32 scale, i32 0x4b400000 - sum q) [m][inter/128] |
+//   hp f32 [m][inter] (h after the transform's first four butterfly stages,
+//   per 128-block element e at 4 (e mod 32) + e / 32)
 struct FfnWorkspace {
-    size_t qx, sx, h, qh, sh, counters, ybuf, err, sync, hst, hsn, total;
+    size_t qx, sx, h, qh, sh, counters, ybuf, err, sync, hst, hsn, hp, total;
 };
 
 FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
@@ -57,6 +59,7 @@ FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
     w.sync = off; off = round_up(off + static_cast<size_t>(2 + (inter + 1023) / 1024) * 4, kWsAlign);
     w.hst = off; off = round_up(off + static_cast<size_t>(m * inter), kWsAlign);
     w.hsn = off; off = round_up(off + static_cast<size_t>(m * (inter / 128)) * 8, kWsAlign);
+    w.hp = off;  off = round_up(off + static_cast<size_t>(m * inter) * 4, kWsAlign);
     w.total = off;
     return w;
 }
@@ -74,6 +77,7 @@ struct FfnPtrs {
     unsigned *segready;
     uint8_t *hst;
     float2 *hsn;
+    float *hp;
 };
 
 FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
@@ -83,7 +87,7 @@ FfnPtrs ffn_ptrs(void *ws, const FfnWorkspace &L) {
                    reinterpret_cast<float *>(b + L.sh), reinterpret_cast<unsigned *>(b + L.counters),
                    reinterpret_cast<float *>(b + L.ybuf), reinterpret_cast<unsigned *>(b + L.err),
                    reinterpret_cast<unsigned long long *>(b + L.sync), reinterpret_cast<unsigned *>(b + L.sync) + 2, b + L.hst,
-                   reinterpret_cast<float2 *>(b + L.hsn)};
+                   reinterpret_cast<float2 *>(b + L.hsn), reinterpret_cast<float *>(b + L.hp)};
 }
 
 tq_status check_weight(const tq_weight *w) {
@@ -167,6 +171,7 @@ void set_ws_rows(tq::Call &c, const FfnPtrs &P, int r0, int hidden, int inter) {
     c.sh = P.sh + static_cast<size_t>(r0) * (inter / 128);
     c.hst = P.hst + static_cast<size_t>(r0) * inter;
     c.hsn = P.hsn + static_cast<size_t>(r0) * (inter / 128);
+    c.hp = P.hp + static_cast<size_t>(r0) * inter;
     c.hcount = P.counters;
     c.ticket = P.ticket;
     c.segready = P.segready;

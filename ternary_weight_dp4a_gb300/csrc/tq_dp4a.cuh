@@ -5,13 +5,16 @@
 // products, converted to fp32 exactly (|d| < 2^22).
 //
 // 2-bit: codes 0, 1, 2 (weights 0, +1, -1) decode to the biased bytes
-// w + 1 = 1, 2, 0, one prmt per four codes: even codes of a word (bits
-// 4i..4i+1) as selector nibbles w & 0x33333333 pick byte c of
-// kTableA = {1, 2, 0}; odd codes (bits 4i+2..4i+3) as nibbles of
-// w & 0xcccccccc are 0, 4 or 8: byte 0 of kTableA (1), byte 0 of kTableB (2),
-// or byte 0 of kTableA in sign-replicate mode (0).  The bias leaves the block
-// exactly: d = sum((w+1)*q) - sum(q).  A word of codes 0..15 gives the dp4a
-// operands of weights [0 2 4 6], [8 10 12 14], [1 3 5 7], [9 11 13 15].
+// w + 1 = 1, 2, 0, one prmt per four codes.  A selector nibble holding two
+// codes (c_hi at bits 2-3, c_lo at bits 0-1) picks byte 4 * (c_hi & 1) + c_lo
+// of the pool {kTableB : kTableA} = {2 2 2 2 : 1 1 1 1}, or, for c_hi = 2 (bit
+// 3), that byte's sign replicated: 0.  Every byte of a table half is the
+// same, so c_lo does not matter and the nibble decodes c_hi: w itself decodes
+// the odd codes of its low half, w >> 16 those of its high half, w << 2 and
+// w >> 14 (each even code moved to the top of a nibble) the even ones.  The
+// bias leaves the block exactly: d = sum((w+1)*q) - sum(q).  A word of codes
+// 0..15 gives the dp4a operands of weights [0 2 4 6], [8 10 12 14],
+// [1 3 5 7], [9 11 13 15].
 // 1-bit: bit e of a row's block is weight e (1 -> +1, 0 -> -1); register s
 // (0..7) of a word holds bits s, 8+s, 16+s, 24+s as bytes 0/1 and
 // d = 2*sum(b*q) - sum(q).
@@ -26,16 +29,15 @@ namespace tq {
 constexpr int kTileRows = 16;       // weight rows per unit
 constexpr int kSegBlocks = 8;       // 128-blocks per segment (fold order)
 
-constexpr uint32_t kTableA = 0x00000201u;
-constexpr uint32_t kTableB = 0x00000002u;
+constexpr uint32_t kTableA = 0x01010101u;
+constexpr uint32_t kTableB = 0x02020202u;
 
 __device__ __forceinline__ void decode_t2(uint32_t w, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                           uint32_t &r3) {
-    const uint32_t e = w & 0x33333333u, o = w & 0xccccccccu;
-    r0 = prmt(kTableA, kTableB, e);
-    r1 = prmt(kTableA, kTableB, e >> 16);
-    r2 = prmt(kTableA, kTableB, o);
-    r3 = prmt(kTableA, kTableB, o >> 16);
+    r0 = prmt(kTableA, kTableB, w << 2);
+    r1 = prmt(kTableA, kTableB, w >> 14);
+    r2 = prmt(kTableA, kTableB, w);
+    r3 = prmt(kTableA, kTableB, w >> 16);
 }
 
 // Position of element e (0..127) of a block in its staged 128 bytes.

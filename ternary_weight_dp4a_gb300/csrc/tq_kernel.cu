@@ -255,6 +255,7 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.sh = c.sh;
     a.hst = c.hst;
     a.hsn = c.hsn;
+    a.hp = c.hp;
     a.hcount = c.hcount;
     a.bst = c.bst;
     a.bsn = c.bsn;

@@ -111,6 +111,8 @@ struct KArgs {
     float *sh;
     uint8_t *hst;             // h staged for phase B: [inter/128][M][128] int8
     float2 *hsn;              // [inter/128][M] (scale, magic - sum q as int bits)
+    float *hp;                // [M][inter]: h after spans 1..8 of the transform, per block
+                              // element e at 4 (e mod 32) + e / 32
     unsigned *hcount;         // rows of each 128-block of h published; zero on entry and on exit
     // phase B input: staged (bst/bsn, as phase A's rotation writes them) or
     // plain int8 qb [M][kB] + fp32 sb [M][kB/128]
@@ -187,29 +189,115 @@ __device__ __forceinline__ float2 block_sn(float sc, int sum) {
     return make_float2(sc, __int_as_float(kMagic - sum));
 }
 
-// Stage one quantised block of row r (lane l holds elements l, l+32, l+64,
-// l+96 as q[0..3]) at blk = act + (b*M + r)*128; returns sum(q) over the warp.
+// Element of a block at staged position p (the inverse of staged_pos).
 template <int FMT>
-__device__ __forceinline__ int stage_block_lanes(const int8_t q[4], int lane, uint8_t *blk) {
-    int sum = 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        blk[staged_pos<FMT>(lane + 32 * c)] = static_cast<uint8_t>(q[c]);
-        sum += q[c];
+__device__ __forceinline__ int staged_elem(int p) {
+    if (FMT == 0) {
+        const int q = p & 15, g = q >> 2;
+        return (p & ~15) + (((g & 1) << 3) | ((q & 3) << 1) | (g >> 1));
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    return sum;
+    return (p & ~31) + 8 * (p & 3) + ((p >> 2) & 7);
 }
 
-// Rotate + quantise rows of bf16 values (in_fn(r, i) gives element i of row
-// r as a float) into the staged layout, up to kRotGroup blocks per warp at a
-// time so their shuffle chains overlap; CTA 0 also writes the plain copy.
+// One butterfly stage of the 128-point transform on values held in staged
+// order (lane l holds staged positions 4l..4l+3 in v[0..3]).  The stage's
+// element span maps to a lane bit (xor mask lm) or to a bit of the register
+// index (rm); the element with the bit clear keeps a + b, the other a - b.
+__device__ __forceinline__ void wht_stage(float (&v)[4], int lane, int lm, int rm) {
+    if (lm != 0) {
+        const bool upper = (lane & lm) != 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[c], lm);
+            v[c] = upper ? __fsub_rn(other, v[c]) : __fadd_rn(v[c], other);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if ((c & rm) == 0) {
+                const float x = v[c], y = v[c | rm];
+                v[c] = __fadd_rn(x, y);
+                v[c | rm] = __fsub_rn(x, y);
+            }
+    }
+}
+
+// The transform's final scale by (float)(1/sqrt(128)), then s = absmax / 127
+// and q = round-half-even(v / s) clamped to [-127, 127] (all q = 0 and s = 0
+// for an all-zero block) over the warp's 128 values, 4 per lane.  Returns s;
+// sum gets the block's sum of codes (every lane).
+__device__ __forceinline__ float scale_quant4(float (&v)[4], int8_t (&q)[4], int &sum) {
+    const float cs = __uint_as_float(0x3db504f3u);  // (float)(1/sqrt(128))
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = __fmul_rn(v[c], cs);
+    // absmax: the order of non-negative floats is that of their bit patterns
+    const float lmax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(lmax)));
+    const float sc = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
+    int lsum = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        int t = 0;
+        if (amax != 0.0f) {
+            t = __float2int_rn(__fdiv_rn(v[c], sc));
+            t = t > 127 ? 127 : (t < -127 ? -127 : t);
+        }
+        q[c] = static_cast<int8_t>(t);
+        lsum += t;
+    }
+    sum = __reduce_add_sync(0xffffffffu, lsum);
+    return sc;
+}
+
+// Rotate and quantise one block held in staged order (lane l holds staged
+// positions 4l..4l+3 in v): the transform's stages in element-span order,
+// then scale_quant4.  word gets the lane's four codes as four consecutive
+// staged bytes.
+template <int FMT>
+__device__ __forceinline__ float rotq_staged(float (&v)[4], int lane, int8_t (&q)[4], uint32_t &word, int &sum) {
+    // element span 1, 2, ..., 64 -> (lane xor mask, register bit)
+    constexpr int kLm[2][7] = {{2, 0, 0, 1, 4, 8, 16}, {1, 2, 4, 0, 0, 8, 16}};
+    constexpr int kRm[2][7] = {{0, 1, 2, 0, 0, 0, 0}, {0, 0, 0, 1, 2, 0, 0}};
+#pragma unroll
+    for (int st = 0; st < 7; ++st) wht_stage(v, lane, kLm[FMT][st], kRm[FMT][st]);
+    const float sc = scale_quant4(v, q, sum);
+    word = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) word |= (static_cast<uint32_t>(static_cast<uint8_t>(q[c]))) << (8 * c);
+    return sc;
+}
+
+// Load, in staged order, the four bf16 values of block row `row` (bf16
+// [.][n]) lane l rotates: 2-bit staged positions 4l..4l+3 are elements b,
+// b+2, b+4, b+6 of the 16-group l/4 (b in {0, 8, 1, 9}), the low or high
+// halves of one aligned 16-byte word; 1-bit ones are strided by 8.
+template <int FMT>
+__device__ __forceinline__ void load_staged_bf16(const uint16_t *blk, int lane, float (&v)[4], bool cached) {
+    if (FMT == 0) {
+        const int g = lane & 3, b = ((g & 1) << 3) | (g >> 1);
+        const uint4 *src = reinterpret_cast<const uint4 *>(blk + (lane >> 2) * 16 + (b & 8));
+        const uint4 w = cached ? __ldg(src) : __ldcg(src);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            v[c] = bf16_bits_to_f32(static_cast<uint16_t>((b & 1) ? (ws[c] >> 16) : (ws[c] & 0xffffu)));
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            v[c] = bf16_bits_to_f32(cached ? __ldg(blk + staged_elem<FMT>(4 * lane + c)) : __ldcg(blk + staged_elem<FMT>(4 * lane + c)));
+    }
+}
+
+// Rotate + quantise rows into the staged layout, up to kRotGroup blocks per
+// warp at a time so their shuffle chains overlap; load(r, b, v) fills v with
+// the four values of block b of row r that this lane holds in staged order
+// (rotq_staged).  CTA 0 also writes the plain copy q_out [rows][k] (natural
+// order) and s_out [rows][k/128].
 constexpr int kRotGroup = 3;
 
-template <int FMT, int M, typename InFn>
-__device__ __forceinline__ void stage_rotated(InFn in_fn, int k, uint8_t *act, float2 *sn, int warp,
-                                              int lane, int8_t *q_out, float *s_out, int r_only = -1) {
+template <int FMT, int M, typename LoadFn>
+__device__ __forceinline__ void stage_rotated(LoadFn load, int k, uint8_t *act, float2 *sn, int warp, int lane,
+                                              int8_t *q_out, float *s_out, int r_only = -1) {
     const int nb = k / kBlock;
     const int rows = r_only >= 0 ? 1 : M;
     for (int blk0 = warp; blk0 < rows * nb; blk0 += kRotGroup * kConsumerWarps) {
@@ -219,25 +307,28 @@ __device__ __forceinline__ void stage_rotated(InFn in_fn, int k, uint8_t *act, f
             const int blk = blk0 + u * kConsumerWarps;
             const int r = r_only >= 0 ? r_only : blk / nb;
             const int b = r_only >= 0 ? blk : blk - r * nb;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) v[u][c] = blk < rows * nb ? in_fn(r, b * kBlock + lane + 32 * c) : 0.0f;
+            if (blk < rows * nb) load(r, b, v[u]);
+            else v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.0f;
         }
+        int8_t q[kRotGroup][4];
+        uint32_t word[kRotGroup];
+        int sum[kRotGroup];
+        float sc[kRotGroup];
 #pragma unroll
-        for (int u = 0; u < kRotGroup; ++u) wht128_warp(v[u], lane);
+        for (int u = 0; u < kRotGroup; ++u) sc[u] = rotq_staged<FMT>(v[u], lane, q[u], word[u], sum[u]);
 #pragma unroll
         for (int u = 0; u < kRotGroup; ++u) {
             const int blk = blk0 + u * kConsumerWarps;
             if (blk >= rows * nb) break;
             const int r = r_only >= 0 ? r_only : blk / nb;
             const int b = r_only >= 0 ? blk : blk - r * nb;
-            int8_t q[4];
-            const float sc = quant_block_warp(v[u], q);
-            const int sum = stage_block_lanes<FMT>(q, lane, act + static_cast<size_t>(b * M + r) * kBlock);
-            if (lane == 0) sn[b * M + r] = block_sn(sc, sum);
+            *reinterpret_cast<uint32_t *>(act + static_cast<size_t>(b * M + r) * kBlock + 4 * lane) = word[u];
+            if (lane == 0) sn[b * M + r] = block_sn(sc[u], sum[u]);
             if (q_out != nullptr) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) q_out[static_cast<size_t>(r) * k + b * kBlock + lane + 32 * c] = q[c];
-                if (lane == 0) s_out[static_cast<size_t>(r) * nb + b] = sc;
+                for (int c = 0; c < 4; ++c)
+                    q_out[static_cast<size_t>(r) * k + b * kBlock + staged_elem<FMT>(4 * lane + c)] = q[u][c];
+                if (lane == 0) s_out[static_cast<size_t>(r) * nb + b] = sc[u];
             }
         }
     }
@@ -461,39 +552,6 @@ __device__ __forceinline__ void unit_advance(UnitPos &u, int step, int extent) {
     }
 }
 
-// Element of a block at staged position p (the inverse of staged_pos).
-template <int FMT>
-__device__ __forceinline__ int staged_elem(int p) {
-    if (FMT == 0) {
-        const int q = p & 15, g = q >> 2;
-        return (p & ~15) + (((g & 1) << 3) | ((q & 3) << 1) | (g >> 1));
-    }
-    return (p & ~31) + 8 * (p & 3) + ((p >> 2) & 7);
-}
-
-// One butterfly stage of the 128-point transform on values held in staged
-// order (lane l holds staged positions 4l..4l+3 in v[0..3]).  The stage's
-// element span maps to a lane bit (xor mask lm) or to a bit of the register
-// index (rm); the element with the bit clear keeps a + b, the other a - b.
-__device__ __forceinline__ void wht_stage(float (&v)[4], int lane, int lm, int rm) {
-    if (lm != 0) {
-        const bool upper = (lane & lm) != 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[c], lm);
-            v[c] = upper ? __fsub_rn(other, v[c]) : __fadd_rn(v[c], other);
-        }
-    } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if ((c & rm) == 0) {
-                const float x = v[c], y = v[c | rm];
-                v[c] = __fadd_rn(x, y);
-                v[c | rm] = __fsub_rn(x, y);
-            }
-    }
-}
-
 // Rotate and quantise 128-block hb of h (all M rows, every row of it
 // published).  The transform runs in the staged order phase B reads: the
 // stages go in element-span order 1, 2, ..., 64, each elementwise, so the
@@ -505,59 +563,27 @@ __device__ __forceinline__ void wht_stage(float (&v)[4], int lane, int lm, int r
 template <int FMT, int M>
 __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, int lane) {
     const int nbh = n / kBlock;
+    // hp holds the block after spans 1..8 (applied by the warps that folded
+    // its tiles); lane l reads elements l, l+32, l+64, l+96
     float v[M][4];
-    if (FMT == 0) {
-        // staged positions 4l..4l+3 hold elements b, b+2, b+4, b+6 of the
-        // 16-group l/4, b in {0, 8, 1, 9}: the low or high halves of one
-        // aligned 16-byte word of h
-        const int g = lane & 3, b = ((g & 1) << 3) | (g >> 1);
 #pragma unroll
-        for (int rr = 0; rr < M; ++rr) {
-            const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(a.h + static_cast<size_t>(rr) * n + hb * kBlock +
-                                                                   (lane >> 2) * 16 + (b & 8)));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                v[rr][c] = bf16_bits_to_f32(static_cast<uint16_t>((b & 1) ? (ws[c] >> 16) : (ws[c] & 0xffffu)));
-        }
-    } else {
-#pragma unroll
-        for (int rr = 0; rr < M; ++rr)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                v[rr][c] = bf16_bits_to_f32(__ldcg(a.h + static_cast<size_t>(rr) * n + hb * kBlock + staged_elem<FMT>(4 * lane + c)));
+    for (int rr = 0; rr < M; ++rr) {
+        const float4 w = __ldcg(reinterpret_cast<const float4 *>(a.hp + static_cast<size_t>(rr) * n + hb * kBlock) + lane);
+        v[rr][0] = w.x; v[rr][1] = w.y; v[rr][2] = w.z; v[rr][3] = w.w;
     }
-    // element span 1, 2, ..., 64 -> (lane xor mask, register bit)
-    constexpr int kLm[2][7] = {{2, 0, 0, 1, 4, 8, 16}, {1, 2, 4, 0, 0, 8, 16}};
-    constexpr int kRm[2][7] = {{0, 1, 2, 0, 0, 0, 0}, {0, 0, 0, 1, 2, 0, 0}};
-    const float cs = __uint_as_float(0x3db504f3u);  // (float)(1/sqrt(128))
     int8_t q[M][4];
     float sc[M];
 #pragma unroll
     for (int rr = 0; rr < M; ++rr) {
+        // spans 16 (lane bit 4), 32 and 64 (register bits 0 and 1)
+        wht_stage(v[rr], lane, 16, 0);
+        wht_stage(v[rr], lane, 0, 1);
+        wht_stage(v[rr], lane, 0, 2);
+        int sum;
+        sc[rr] = scale_quant4(v[rr], q[rr], sum);
+        uint8_t *hst = a.hst + static_cast<size_t>(hb * M + rr) * kBlock;
 #pragma unroll
-        for (int st = 0; st < 7; ++st) wht_stage(v[rr], lane, kLm[FMT][st], kRm[FMT][st]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[rr][c] = __fmul_rn(v[rr][c], cs);
-        // absmax over the block: the order of non-negative floats is that of their bits
-        const float lmax = fmaxf(fmaxf(fabsf(v[rr][0]), fabsf(v[rr][1])), fmaxf(fabsf(v[rr][2]), fabsf(v[rr][3])));
-        const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(lmax)));
-        sc[rr] = amax == 0.0f ? 0.0f : __fdiv_rn(amax, 127.0f);
-        int sum = 0;
-        uint32_t word = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            int t = 0;
-            if (amax != 0.0f) {
-                t = __float2int_rn(__fdiv_rn(v[rr][c], sc[rr]));
-                t = t > 127 ? 127 : (t < -127 ? -127 : t);
-            }
-            q[rr][c] = static_cast<int8_t>(t);
-            sum += t;
-            word |= (static_cast<uint32_t>(t) & 0xffu) << (8 * c);
-        }
-        sum = __reduce_add_sync(0xffffffffu, sum);
-        *reinterpret_cast<uint32_t *>(a.hst + static_cast<size_t>(hb * M + rr) * kBlock + 4 * lane) = word;
+        for (int c = 0; c < 4; ++c) hst[staged_pos<FMT>(lane + 32 * c)] = static_cast<uint8_t>(q[rr][c]);
         if (lane == 0) a.hsn[hb * M + rr] = block_sn(sc[rr], sum);
     }
     __syncwarp();
@@ -568,8 +594,7 @@ __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, in
 #pragma unroll
     for (int rr = 0; rr < M; ++rr) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            a.qh[static_cast<size_t>(rr) * n + hb * kBlock + staged_elem<FMT>(4 * lane + c)] = q[rr][c];
+        for (int c = 0; c < 4; ++c) a.qh[static_cast<size_t>(rr) * n + hb * kBlock + lane + 32 * c] = q[rr][c];
         if (lane == 0) a.sh[static_cast<size_t>(rr) * nbh + hb] = sc[rr];
     }
     if (lane == 0) a.hcount[hb] = 0u;
@@ -724,8 +749,9 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
         const int hidden = ga.k;
         if (a.in_mode == kInRotX) {
             const uint16_t *x = a.x;
-            stage_rotated<FMT, M>([&](int r, int i) { return bf16_bits_to_f32(x[static_cast<size_t>(r) * hidden + i]); },
-                                  hidden, act_x, sn_x, warp, lane, cta == 0 ? a.qx : nullptr, a.sx);
+            stage_rotated<FMT, M>([&](int r, int b, float (&v)[4]) {
+                load_staged_bf16<FMT>(x + static_cast<size_t>(r) * hidden + b * kBlock, lane, v, false);
+            }, hidden, act_x, sn_x, warp, lane, cta == 0 ? a.qx : nullptr, a.sx);
         } else if (a.in_mode == kInNormY) {
             for (int r = 0; r < M; ++r) {
                 // 1/rms: 256 partial sums (thread i adds y[i], y[i+256], ...),
@@ -747,8 +773,11 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 const float ss = __fadd_rn(__fadd_rn(w01, w23), __fadd_rn(w45, w67));
                 const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hidden)), a.eps)));
                 named_barrier(1, kConsumers);
-                stage_rotated<FMT, M>([&](int, int i) {
-                    return bf16_bits_to_f32(f32_to_bf16_bits(__fmul_rn(__ldcg(yr + i), inv)));
+                stage_rotated<FMT, M>([&](int, int b, float (&v)[4]) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[c] = bf16_bits_to_f32(f32_to_bf16_bits(
+                            __fmul_rn(__ldcg(yr + b * kBlock + staged_elem<FMT>(4 * lane + c)), inv)));
                 }, hidden, act_x, sn_x, warp, lane, cta == 0 ? a.qx : nullptr, a.sx, r);
             }
         } else {
@@ -886,22 +915,41 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             const size_t ustride = static_cast<size_t>(in_a ? 1 : P.count) * M * kTileRows;
             float *pt = (in_a ? part_a + static_cast<size_t>(lt) * P.upt * M * kTileRows : part_b + static_cast<size_t>(lt) * M * kTileRows) +
                         r * kTileRows + rr16;
-            for (int ra = r; ra < M; ra += 2) {
-                float *pr = pt + (ra - r) * kTileRows;
+            for (int k2 = 0; 2 * k2 < M; ++k2) {
+                const int ra = r + 2 * k2;
+                const bool act = ra < M;
+                float *pr = pt + 2 * k2 * kTileRows;
                 if (in_a) {
-                    const float gv = fold_tree(pr, P.nseg, static_cast<int>(ustride));
-                    const float uv = fold_tree(pr + P.nseg * ustride, P.nseg, static_cast<int>(ustride));
-                    if (row < P.n)
-                        a.h[static_cast<size_t>(ra) * P.n + row] = f32_to_bf16_bits(__fmul_rn(tq_silu(gv), uv));
-                } else {
+                    uint16_t hv = 0;
+                    if (act) {
+                        const float gv = fold_tree(pr, P.nseg, static_cast<int>(ustride));
+                        const float uv = fold_tree(pr + P.nseg * ustride, P.nseg, static_cast<int>(ustride));
+                        hv = f32_to_bf16_bits(__fmul_rn(tq_silu(gv), uv));
+                        if (row < P.n) a.h[static_cast<size_t>(ra) * P.n + row] = hv;
+                    }
+                    if (a.rotate_h) {
+                        // the transform's spans 1, 2, 4, 8 stay inside the
+                        // tile's 16 rows (lanes of one half-warp): apply them
+                        // here, for the block's owner to finish
+                        float pv = bf16_bits_to_f32(hv);
+#pragma unroll
+                        for (int sp = 1; sp < kTileRows; sp <<= 1) {
+                            const float other = __shfl_xor_sync(0xffffffffu, pv, sp);
+                            pv = (rr16 & sp) ? __fsub_rn(other, pv) : __fadd_rn(pv, other);
+                        }
+                        const int e = (tile % kTilesPerHBlock) * kTileRows + rr16;
+                        if (act)
+                            a.hp[static_cast<size_t>(ra) * P.n + (tile / kTilesPerHBlock) * kBlock + 4 * (e & 31) + (e >> 5)] = pv;
+                    }
+                } else if (act) {
                     const float yv = fold_tree(pr, P.nseg, static_cast<int>(ustride));
                     if (row < P.n) a.y[static_cast<size_t>(ra) * P.n + row] = yv;
                 }
             }
             if (in_a && a.rotate_h) {
-                // publish the tile's rows of h: a gpu-scope fence (cumulative
-                // over the warp's stores), then a fire-and-forget add of its
-                // rows to the block's count.  Only this warp waits for the
+                // publish the tile's rows of h and hp: a gpu-scope fence
+                // (cumulative over the warp's stores), then a fire-and-forget
+                // add of its rows to the block's count.  Only this warp waits for the
                 // fence; the others keep claiming units.
                 __syncwarp();
                 if (lane == 0) {

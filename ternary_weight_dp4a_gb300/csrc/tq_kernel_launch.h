@@ -35,6 +35,7 @@ struct Call {
     float *sh;
     uint8_t *hst;                       // h staged for phase B (written with qh)
     float2 *hsn;
+    float *hp;                          // h after its first four butterfly stages (rotate_h)
     unsigned *hcount;
     const uint8_t *bst;                 // phase B input, staged; or plain qb/sb
     const float2 *bsn;

@@ -20,7 +20,8 @@ constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // The FFN workspace at the largest sizes, laid out as tq_ffn_step lays it out
 // (every section 256-byte aligned): qx, sx, h, qh, sh, counters, ybuf, err,
-// sync counters, staged h and its (scale, magic - sum) pairs.
+// sync counters, staged h and its (scale, magic - sum) pairs, h after the
+// first butterfly stages.
 constexpr size_t kStaticBytes =
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden) +
     align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxHidden / 128) * 4) +
@@ -31,7 +32,8 @@ constexpr size_t kStaticBytes =
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden * 4) + align256(4) +
     align256(static_cast<size_t>(2 + kStaticMaxInter / 1024) * 4) +
     align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
-    align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 8);
+    align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 8) +
+    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter * 4);
 
 // One copy per GPU that loads the library, held until the process exits.
 // Device code could name it directly; host code must use the address from

@@ -23,7 +23,8 @@ def ws_offsets(m, hidden, inter):
     for name, nbytes in (("qx", m * hidden), ("sx", m * (hidden // B) * 4),
                          ("h", m * inter * 2), ("qh", m * inter), ("sh", m * (inter // B) * 4),
                          ("counters", (inter // B) * 4), ("ybuf", m * hidden * 4), ("err", 4),
-                         ("sync", (2 + (inter + 1023) // 1024) * 4), ("hst", m * inter), ("hsn", m * (inter // B) * 8)):
+                         ("sync", (2 + (inter + 1023) // 1024) * 4), ("hst", m * inter), ("hsn", m * (inter // B) * 8),
+                         ("hp", m * inter * 4)):
         o[name] = off
         off = round_up(off + nbytes, 256)
     o["total"] = off

@@ -41,9 +41,10 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     # qx 5120 | sx 160->256 | h 34816 | qh 17408 | sh 544->768 | counters 544->768 |
-    # ybuf 20480 | err 4->256 | sync 76->256 | hst 17408 | hsn 1088->1280, each 256-aligned
+    # ybuf 20480 | err 4->256 | sync 76->256 | hst 17408 | hsn 1088->1280 | hp 69632,
+    # each 256-aligned
     assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == \
-        5120 + 256 + 34816 + 17408 + 768 + 768 + 20480 + 256 + 256 + 17408 + 1280
+        5120 + 256 + 34816 + 17408 + 768 + 768 + 20480 + 256 + 256 + 17408 + 1280 + 69632
     assert lib.tq_ffn_workspace_bytes(0, 5120, 17408) == 0
 
 
