@@ -350,22 +350,23 @@ __device__ __forceinline__ float fold_tree(float *V, int cnt, int stride) {
     return V[0];
 }
 
-// One 128-block of a unit: decode, four MMAs, exact block dot, and the
-// fold step t_b into the segment sums of weight rows g and g+8.
 // One unit: 16 weight rows x the segment's blocks.  Lane l = 16h + r works
 // on row r, half h of every block (2-bit: words 4h..4h+3, 64 weights; 1-bit:
 // words 2h, 2h+1); each code word feeds its own dp4a chain, the chains and
 // the two halves meet in adds and one shuffle, and lane r (h = 0) folds
 // t_b = (float)d * (ws * sa) into the segment sums acc[mm] in ascending block
-// order.  dots (may be null) receives every block dot.
-template <int FMT, int M>
+// order.  dots (may be null) receives every block dot.  FAST: a full
+// segment, no dots, 2-bit codes in the 3D layout (the common case, compiled
+// without the per-block checks).
+template <int FMT, int M, bool FAST>
 __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
                                           int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
                                           int32_t *dots, int row, int n, int nb) {
     const int r = lane & 15, h = lane >> 4;
+    if (FAST) codes3d = true;
 #pragma unroll
     for (int bl = 0; bl < kSegBlocks; ++bl) {
-        if (bl >= bcount) break;
+        if (!FAST && bl >= bcount) break;
         const int b = b0 + bl;
         int dot[M];
         const uint8_t *ab = act + static_cast<size_t>(b) * M * kBlock + h * 64;
@@ -426,7 +427,8 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
             const float2 sv = sn[b * M + mm];                // (activation scale, magic - sum q)
             const float v = int_to_float_exact(d, __float_as_int(sv.y));
             acc[mm] = __fadd_rn(acc[mm], __fmul_rn(v, __fmul_rn(ws, sv.x)));
-            if (dots != nullptr && h == 0 && row < n) dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
+            if (!FAST && dots != nullptr && h == 0 && row < n)
+                dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
         }
     }
 }
@@ -887,8 +889,13 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             float acc[M];
 #pragma unroll
             for (int mm = 0; mm < M; ++mm) acc[mm] = 0.0f;
-            unit_dp4a<FMT, M>(cs, md.codes3d != 0, in_a ? act_x : act_h, in_a ? sn_x : sn_h, seg * kSegBlocks,
-                              bcount, wsr, lane, acc, in_a ? nullptr : a.dots, row, P.n, P.nb);
+            int32_t *const dots = in_a ? nullptr : a.dots;
+            if (bcount == kSegBlocks && dots == nullptr && (FMT == 1 || md.codes3d))
+                unit_dp4a<FMT, M, true>(cs, true, in_a ? act_x : act_h, in_a ? sn_x : sn_h, seg * kSegBlocks,
+                                        bcount, wsr, lane, acc, nullptr, row, P.n, P.nb);
+            else
+                unit_dp4a<FMT, M, false>(cs, md.codes3d != 0, in_a ? act_x : act_h, in_a ? sn_x : sn_h,
+                                         seg * kSegBlocks, bcount, wsr, lane, acc, dots, row, P.n, P.nb);
             // the slot's codes and scales are all in registers: hand it back
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
