@@ -350,10 +350,11 @@ __device__ __forceinline__ float fold_tree(float *V, int cnt, int stride) {
     return V[0];
 }
 
-// One unit: 16 weight rows x the segment's blocks.  Lane l = 16h + r works
-// on row r, half h of every block (2-bit: words 4h..4h+3, 64 weights; 1-bit:
+// One unit: 16 weight rows x the segment's blocks.  Lane l = 2r + h works
+// on row r, half h of every block (with the 128-byte swizzle, each quarter
+// warp then reads 8 distinct 16-byte bank groups of the codes) (2-bit: words 4h..4h+3, 64 weights; 1-bit:
 // words 2h, 2h+1); each code word feeds its own dp4a chain, the chains and
-// the two halves meet in adds and one shuffle, and lane r (h = 0) folds
+// the two halves meet in adds and one shuffle, and lanes 2r, 2r + 1 fold
 // t_b = (float)d * (ws * sa) into the segment sums acc[mm] in ascending block
 // order.  dots (may be null) receives every block dot.  FAST: a full
 // segment, no dots, 2-bit codes in the 3D layout (the common case, compiled
@@ -362,7 +363,7 @@ template <int FMT, int M, bool FAST>
 __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
                                           int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
                                           int32_t *dots, int row, int n, int nb) {
-    const int r = lane & 15, h = lane >> 4;
+    const int r = lane >> 1, h = lane & 1;
     if (FAST) codes3d = true;
 #pragma unroll
     for (int bl = 0; bl < kSegBlocks; ++bl) {
@@ -422,7 +423,7 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
         const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
 #pragma unroll
         for (int mm = 0; mm < M; ++mm) {
-            int d = dot[mm] + __shfl_xor_sync(0xffffffffu, dot[mm], 16);
+            int d = dot[mm] + __shfl_xor_sync(0xffffffffu, dot[mm], 1);
             if (FMT == 1) d *= 2;
             const float2 sv = sn[b * M + mm];                // (activation scale, magic - sum q)
             const float v = int_to_float_exact(d, __float_as_int(sv.y));
@@ -868,20 +869,20 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             const uint8_t *cs = codes_ring + static_cast<size_t>(slot) * kCodesSlot;
             const int bcount = min(kSegBlocks, P.nb - seg * kSegBlocks);
 
-            // weight scales of row r of the tile for the segment's blocks
-            const int rr16 = lane & 15;
-            const int row = tile * kTileRows + rr16;
+            // weight scales of the lane's row (lane 2r + h: row r of the tile)
+            // for the segment's blocks
+            const int urow = tile * kTileRows + (lane >> 1);
             uint32_t wsr[4];
             if (md.scales_tma) {
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2) + rr16 * 8);
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2) + (lane >> 1) * 8);
                 wsr[0] = u0.x; wsr[1] = u0.y; wsr[2] = u0.z; wsr[3] = u0.w;
             } else {
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     uint32_t lo = 0, hi = 0;
                     const int bb = seg * kSegBlocks + 2 * w;
-                    if (row < P.n && 2 * w < bcount) lo = ldg_u16(md.scales + static_cast<size_t>(row) * P.nb + bb);
-                    if (row < P.n && 2 * w + 1 < bcount) hi = ldg_u16(md.scales + static_cast<size_t>(row) * P.nb + bb + 1);
+                    if (urow < P.n && 2 * w < bcount) lo = ldg_u16(md.scales + static_cast<size_t>(urow) * P.nb + bb);
+                    if (urow < P.n && 2 * w + 1 < bcount) hi = ldg_u16(md.scales + static_cast<size_t>(urow) * P.nb + bb + 1);
                     wsr[w] = lo | (hi << 16);
                 }
             }
@@ -892,19 +893,19 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             int32_t *const dots = in_a ? nullptr : a.dots;
             if (bcount == kSegBlocks && dots == nullptr && (FMT == 1 || md.codes3d))
                 unit_dp4a<FMT, M, true>(cs, true, in_a ? act_x : act_h, in_a ? sn_x : sn_h, seg * kSegBlocks,
-                                        bcount, wsr, lane, acc, nullptr, row, P.n, P.nb);
+                                        bcount, wsr, lane, acc, nullptr, urow, P.n, P.nb);
             else
                 unit_dp4a<FMT, M, false>(cs, md.codes3d != 0, in_a ? act_x : act_h, in_a ? sn_x : sn_h,
-                                         seg * kSegBlocks, bcount, wsr, lane, acc, dots, row, P.n, P.nb);
+                                         seg * kSegBlocks, bcount, wsr, lane, acc, dots, urow, P.n, P.nb);
             // the slot's codes and scales are all in registers: hand it back
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
 
             // segment sums of this unit -> shared memory; count the tile
             float *pu = (in_a ? part_a : part_b) + static_cast<size_t>(i) * M * kTileRows;
-            if (lane < kTileRows) {
+            if ((lane & 1) == 0) {
 #pragma unroll
-                for (int mm = 0; mm < M; ++mm) pu[mm * kTileRows + lane] = acc[mm];
+                for (int mm = 0; mm < M; ++mm) pu[mm * kTileRows + (lane >> 1)] = acc[mm];
             }
             __syncwarp();
             int last = 0;
@@ -919,6 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             // tree and store h (phase A) or y (phase B).  Phase A units of a
             // tile are consecutive; phase B's are `count` apart.
             const int r = lane >> 4;            // activation rows r, r + 2, ... of the tile's 16 outputs
+            const int rr16 = lane & 15;         // output row of the tile
+            const int row = tile * kTileRows + rr16;
             const size_t ustride = static_cast<size_t>(in_a ? 1 : P.count) * M * kTileRows;
             float *pt = (in_a ? part_a + static_cast<size_t>(lt) * P.upt * M * kTileRows : part_b + static_cast<size_t>(lt) * M * kTileRows) +
                         r * kTileRows + rr16;
