@@ -31,8 +31,7 @@
 
 namespace tq {
 
-constexpr int kConsumerWarps = 15;      // 14 compute warps + the epilogue warp
-constexpr int kComputeWarps = kConsumerWarps - 1;
+constexpr int kConsumerWarps = 15;      // compute warps (warp 15 is the producer)
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kCodesSlot = 4096;        // 16 rows x 8 blocks of codes (2-bit: two 2 KB planes)
@@ -795,13 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     // warp claims the next unit from a shared counter when it is free, so a
     // warp that runs slow (or waits for a segment of h) holds up no other
     // warp's units.  A warp's claims increase, so its unit positions and
-    // (slot, round) = divmod(k, S) advance incrementally.  When phase A
-    // rotates h, block hb is rotated by its owner, CTA G - 1 - (hb mod G)
-    // (owners spread one block per CTA as far as the blocks go), on its last
-    // consumer warp; a CTA that owns no block computes units on that warp too.
-    const int nbh = a.do_a ? ga.n / kBlock : 0;
-    const bool epi = a.do_a && a.rotate_h && G - 1 - cta < nbh;
-    const int ncw = epi ? kComputeWarps : kConsumerWarps;
+    // (slot, round) = divmod(k, S) advance incrementally.
+    const int ncw = kConsumerWarps;
     int *tcnt_a = tcnt, *tcnt_b = tcnt + a.tiles_max;
     float *part_a = part, *part_b = part + static_cast<size_t>(ga.units) * M * kTileRows;
     if (warp < ncw) {
@@ -940,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                     if (a.rotate_h) {
                         // the transform's spans 1, 2, 4, 8 stay inside the
                         // tile's 16 rows (lanes of one half-warp): apply them
-                        // here, for the block's owner to finish
+                        // here, for the block's rotator to finish
                         float pv = bf16_bits_to_f32(hv);
 #pragma unroll
                         for (int sp = 1; sp < kTileRows; sp <<= 1) {
@@ -958,39 +952,21 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             }
             if (in_a && a.rotate_h) {
                 // publish the tile's rows of h and hp: a gpu-scope fence
-                // (cumulative over the warp's stores), then a fire-and-forget
-                // add of its rows to the block's count.  Only this warp waits for the
-                // fence; the others keep claiming units.
+                // (cumulative over the warp's stores), then an add of its rows
+                // to the block's count.  The add that completes the block
+                // makes this warp the block's rotator; it acquires the other
+                // tiles' rows and rotates at once.  Only this warp waits; the
+                // others keep claiming units.
                 __syncwarp();
+                int completes = 0;
                 if (lane == 0) {
+                    const unsigned rows = static_cast<unsigned>(min(kTileRows, P.n - tile * kTileRows));
                     fence_acq_rel_gpu();
-                    red_add_relaxed_gpu(&a.hcount[tile / kTilesPerHBlock],
-                                        static_cast<unsigned>(min(kTileRows, P.n - tile * kTileRows)));
+                    completes = atomicAdd(&a.hcount[tile / kTilesPerHBlock], rows) + rows == static_cast<unsigned>(kBlock);
+                    if (completes) fence_acq_rel_gpu();
                 }
+                if (__shfl_sync(0xffffffffu, completes, 0)) rotate_h_block<FMT, M>(a, P.n, tile / kTilesPerHBlock, lane);
             }
-        }
-    } else if (epi) {
-        // ---- owner warp: rotate each owned block of h once all its rows are
-        // published.  Lane 0 polls the block's count; the warp follows its
-        // broadcast.
-        for (int own = G - 1 - cta; own < nbh; own += G) {
-            int ready = 0;
-            if (lane == 0) {
-                const long long t0 = clock64();
-                while (!(ready = ld_relaxed_u32(&a.hcount[own]) == static_cast<unsigned>(kBlock))) {
-                    if (clock64() - t0 > kWaitBudgetCycles) break;
-                    __nanosleep(64);
-                }
-                // acquire: what the rows' publishers released is visible to
-                // lane 0, and through the warp's shuffle to every lane
-                fence_acq_rel_gpu();
-            }
-            if (!__shfl_sync(0xffffffffu, ready, 0)) {
-                ok = false;
-                bad |= 32u;
-                break;
-            }
-            rotate_h_block<FMT, M>(a, ga.n, own, lane);
         }
     }
 
