@@ -161,14 +161,22 @@ __host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int
 
 __device__ __forceinline__ int phase_tile(const PhaseGeo &p, int G, int lt) { return deal_tile(p.deal, G, p.dc, lt); }
 
-// Fire-and-forget add at gpu scope (nothing waits for a returned value).
-__device__ __forceinline__ void red_add_relaxed_gpu(unsigned *p, unsigned v) {
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Release/acquire fence at gpu scope (cumulative: orders what this thread
 // has observed, e.g. its warp's stores before a __syncwarp).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Add with release semantics at gpu scope (fire-and-forget): the writes that
+// precede it (cumulatively) are visible to whoever observes the sum.
+__device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Fetch-and-add with acquire-release semantics at gpu scope.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
     unsigned v;
@@ -364,6 +372,7 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
                                           int32_t *dots, int row, int n, int nb) {
     const int r = lane >> 1, h = lane & 1;
     if (FAST) codes3d = true;
+    (void)codes3d;
 #pragma unroll
     for (int bl = 0; bl < kSegBlocks; ++bl) {
         if (!FAST && bl >= bcount) break;
@@ -559,9 +568,9 @@ __device__ __forceinline__ void unit_advance(UnitPos &u, int step, int extent) {
 // stages go in element-span order 1, 2, ..., 64, each elementwise, so the
 // values are those of the natural-order transform, and each lane's four codes
 // are four consecutive staged bytes (one store).  The staged copy hst/hsn is
-// written first and released (fence, then the block's add to its segment's
-// ready counter when phase B runs in this launch); qh/sh for the caller and
-// the block's count reset come after.
+// written first and released (a release add to its segment's ready counter
+// when phase B runs in this launch); qh/sh for the caller and the block's
+// count reset come after.
 template <int FMT, int M>
 __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, int lane) {
     const int nbh = n / kBlock;
@@ -589,10 +598,7 @@ __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, in
         if (lane == 0) a.hsn[hb * M + rr] = block_sn(sc[rr], sum);
     }
     __syncwarp();
-    if (lane == 0 && a.do_b) {
-        fence_acq_rel_gpu();
-        red_add_relaxed_gpu(a.segready + hb / kSegBlocks, 1u);
-    }
+    if (lane == 0 && a.do_b) red_add_release_gpu(a.segready + hb / kSegBlocks, 1u);
 #pragma unroll
     for (int rr = 0; rr < M; ++rr) {
 #pragma unroll
@@ -951,9 +957,9 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 }
             }
             if (in_a && a.rotate_h) {
-                // publish the tile's rows of h and hp: a gpu-scope fence
-                // (cumulative over the warp's stores), then an add of its rows
-                // to the block's count.  The add that completes the block
+                // publish the tile's rows of h and hp: an acquire-release add
+                // of its rows to the block's count (its release is cumulative
+                // over the warp's stores, ordered before it by __syncwarp).  The add that completes the block
                 // makes this warp the block's rotator; it acquires the other
                 // tiles' rows and rotates at once.  Only this warp waits; the
                 // others keep claiming units.
@@ -961,9 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 int completes = 0;
                 if (lane == 0) {
                     const unsigned rows = static_cast<unsigned>(min(kTileRows, P.n - tile * kTileRows));
-                    fence_acq_rel_gpu();
-                    completes = atomicAdd(&a.hcount[tile / kTilesPerHBlock], rows) + rows == static_cast<unsigned>(kBlock);
-                    if (completes) fence_acq_rel_gpu();
+                    completes = atom_add_acq_rel_gpu(&a.hcount[tile / kTilesPerHBlock], rows) + rows ==
+                                static_cast<unsigned>(kBlock);
                 }
                 if (__shfl_sync(0xffffffffu, completes, 0)) rotate_h_block<FMT, M>(a, P.n, tile / kTilesPerHBlock, lane);
             }
