@@ -246,6 +246,7 @@ __device__ __forceinline__ float scale_quant4(float (&v)[4], int8_t (&q)[4], int
     for (int c = 0; c < 4; ++c) {
         int t = 0;
         if (amax != 0.0f) {
+            // the clamp matters only when absmax / 127 underflows to zero
             t = __float2int_rn(__fdiv_rn(v[c], sc));
             t = t > 127 ? 127 : (t < -127 ? -127 : t);
         }
@@ -945,7 +946,9 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
 #pragma unroll
                         for (int sp = 1; sp < kTileRows; sp <<= 1) {
                             const float other = __shfl_xor_sync(0xffffffffu, pv, sp);
-                            pv = (rr16 & sp) ? __fsub_rn(other, pv) : __fadd_rn(pv, other);
+                            // lower row: rn(a + b) = fma(+1, a, b); upper row:
+                            // rn(b - a) = fma(-1, a, b) (the product is exact)
+                            pv = __fmaf_rn((rr16 & sp) ? -1.0f : 1.0f, pv, other);
                         }
                         const int e = (tile % kTilesPerHBlock) * kTileRows + rr16;
                         if (act)
