@@ -368,7 +368,7 @@ __device__ __forceinline__ float fold_tree(float *V, int cnt, int stride) {
 // segment, no dots, 2-bit codes in the 3D layout (the common case, compiled
 // without the per-block checks).
 template <int FMT, int M, bool FAST>
-__device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
+__device__ __forceinline__ void unit_dp4a_1row(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
                                           int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
                                           int32_t *dots, int row, int n, int nb) {
     const int r = lane >> 1, h = lane & 1;
@@ -441,6 +441,114 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
                 dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
         }
     }
+}
+
+template <int FMT, int M, bool FAST>
+__device__ __forceinline__ void unit_dp4a_rows(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
+                                          int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
+                                          int32_t *dots, int row, int n, int nb) {
+    const int r = lane >> 1, h = lane & 1;
+    if (FAST) codes3d = true;
+    (void)codes3d;
+#pragma unroll
+    for (int bl = 0; bl < kSegBlocks; ++bl) {
+        if (!FAST && bl >= bcount) break;
+        const int b = b0 + bl;
+        int dot[M];
+        float2 sv[M];                                        // (activation scale, magic - sum q)
+#pragma unroll
+        for (int mm = 0; mm < M; ++mm) sv[mm] = sn[b * M + mm];
+        const uint8_t *ab = act + static_cast<size_t>(b) * M * kBlock + h * 64;
+        if constexpr (FMT == 0) {
+            // 128-byte line of (row r, plane bl/4): 3D copies lay rows out
+            // [row][plane], 2D copies [plane][row]; the swizzle XORs the
+            // 16-byte chunk with the line index mod 8
+            const int line = codes3d ? 2 * r + (bl >> 2) : (bl >> 2) * kTileRows + r;
+            const uint4 cw = *reinterpret_cast<const uint4 *>(cs + line * 128 +
+                                                              ((((bl & 3) * 2 + h) ^ (line & 7)) * 16));
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            // two dp4a chains per row (words 0-1, words 2-3); the h = 0 half's
+            // first chain starts from the block's magic - sum q, so the halves'
+            // sum is the biased value the exact conversion needs
+            constexpr int kChains = 2;
+            int part[M][kChains];
+#pragma unroll
+            for (int mm = 0; mm < M; ++mm) {
+                part[mm][0] = h == 0 ? __float_as_int(sv[mm].y) : 0;
+#pragma unroll
+                for (int ch = 1; ch < kChains; ++ch) part[mm][ch] = 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t p0, p1, p2, p3;
+                decode_t2(words[i], p0, p1, p2, p3);
+#pragma unroll
+                for (int mm = 0; mm < M; ++mm) {
+                    const uint4 av = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 16);
+                    int d = part[mm][i * kChains / 4];
+                    d = __dp4a(static_cast<int>(p0), static_cast<int>(av.x), d);
+                    d = __dp4a(static_cast<int>(p1), static_cast<int>(av.y), d);
+                    d = __dp4a(static_cast<int>(p2), static_cast<int>(av.z), d);
+                    part[mm][i * kChains / 4] = __dp4a(static_cast<int>(p3), static_cast<int>(av.w), d);
+                }
+            }
+#pragma unroll
+            for (int mm = 0; mm < M; ++mm) {
+                int sum = part[mm][0];
+#pragma unroll
+                for (int ch = 1; ch < kChains; ++ch) sum += part[mm][ch];
+                dot[mm] = sum;
+            }
+        } else {
+            const uint2 cw = *reinterpret_cast<const uint2 *>(cs + r * 128 + ((bl ^ (r & 7)) * 16) + h * 8);
+            const uint32_t words[2] = {cw.x, cw.y};
+            int part[M][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+#pragma unroll
+                for (int mm = 0; mm < M; ++mm) {
+                    const uint4 a0 = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 32);
+                    const uint4 a1 = *reinterpret_cast<const uint4 *>(ab + mm * kBlock + i * 32 + 16);
+                    const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    int d0 = 0, d1 = 0;
+#pragma unroll
+                    for (int sb = 0; sb < 8; sb += 2) {
+                        d0 = __dp4a(static_cast<int>((words[i] >> sb) & 0x01010101u), static_cast<int>(av[sb]), d0);
+                        d1 = __dp4a(static_cast<int>((words[i] >> (sb + 1)) & 0x01010101u), static_cast<int>(av[sb + 1]), d1);
+                    }
+                    part[mm][2 * i] = d0;
+                    part[mm][2 * i + 1] = d1;
+                }
+            }
+#pragma unroll
+            for (int mm = 0; mm < M; ++mm) dot[mm] = (part[mm][0] + part[mm][1]) + (part[mm][2] + part[mm][3]);
+        }
+        const uint32_t wsw = wsr[bl >> 1];
+        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
+#pragma unroll
+        for (int mm = 0; mm < M; ++mm) {
+            const int d = dot[mm] + __shfl_xor_sync(0xffffffffu, dot[mm], 1);
+            // 2-bit: d already holds magic - sum; 1-bit: 2 d + (magic - sum)
+            const int biased = FMT == 0 ? d : 2 * d + __float_as_int(sv[mm].y);
+            const float v = __fsub_rn(__int_as_float(biased), 12582912.0f);   // exact: |d| < 2^22
+            acc[mm] = __fadd_rn(acc[mm], __fmul_rn(v, __fmul_rn(ws, sv[mm].x)));
+            if (!FAST && dots != nullptr && h == 0 && row < n)
+                dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
+        }
+    }
+}
+
+// One unit, dispatched on the row count: one row keeps four short dp4a
+// chains per block (latency); more rows use two longer chains per row and fold
+// the block's magic - sum q into the first (fewer integer adds).
+template <int FMT, int M, bool FAST>
+__device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const uint8_t *act, const float2 *sn,
+                                          int b0, int bcount, const uint32_t (&wsr)[4], int lane, float (&acc)[M],
+                                          int32_t *dots, int row, int n, int nb) {
+    if constexpr (M == 1)
+        unit_dp4a_1row<FMT, M, FAST>(cs, codes3d, act, sn, b0, bcount, wsr, lane, acc, dots, row, n, nb);
+    else
+        unit_dp4a_rows<FMT, M, FAST>(cs, codes3d, act, sn, b0, bcount, wsr, lane, acc, dots, row, n, nb);
 }
 
 // Stage blocks [b_begin, b_end) of int8 rows q [M][k] (+ fp32 s [M][k/128])
