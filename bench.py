@@ -221,6 +221,54 @@ def time_graph(fn_steps, reps: int, warmup_reps: int, world: int, sampler_gpu=No
     return start.elapsed_time(end), clocks
 
 
+# Standalone GEMV shapes (n, k): the tiny config, the FFN's gate/up and down
+# matrices, the full-attention projections of the model family the pages
+# describe (head_dim 256, 8:1 GQA with 2 KV heads: q 16 x 256 = 4096, k and
+# v 2 x 256 = 512 each, o back to 5120), and a wide GEMV at LM-head scale
+# (N = 131072; the pages give no vocabulary size).
+GEMV_SHAPES = (("tiny_n512_k256", 512, 256), ("ffn_gate_n17408_k5120", 17408, 5120),
+               ("ffn_down_n5120_k17408", 5120, 17408), ("attn_q_n4096_k5120", 4096, 5120),
+               ("attn_kv_n512_k5120", 512, 5120), ("attn_o_n5120_k4096", 5120, 4096),
+               ("wide_n131072_k5120", 131072, 5120))
+
+
+def gemv_sweep(peak: float, fmt: int = 0, ms=(1, 8)):
+    """tq_gemv time per call for each shape and row count, graph-replayed over
+    enough independent weight copies to exceed the 129 MB L2 (at most 64
+    copies: the smallest shapes stay partly L2-resident, said per entry)."""
+    import torch
+    from ternary_weight_dp4a_gb300 import synth, tq
+    out = {}
+    l2 = 129 * 2**20
+    for name, n, k in GEMV_SHAPES:
+        wbytes = n * k // (4 if fmt == 0 else 8) + 2 * n * (k // 128)
+        copies = max(1, min(64, -(-2 * l2 // wbytes)))
+        ws = []
+        for c in range(copies):
+            codes, scales = synth.weight(n, k, fmt, 7000 + c, device="cuda")
+            ws.append(tq.pack_weights(codes, fmt, scales))
+            del codes
+        ent = {"n": n, "k": k, "weight_bytes": wbytes, "copies": copies,
+               "l2_resident": copies * wbytes < l2}
+        for m in ms:
+            x = synth.activation(m, k, synth.SEED_ACT_BASE, 0.01, device="cuda")
+            q, sc = tq.rotate_quant(x)
+            y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+
+            def f():
+                for w in ws:
+                    tq.gemv(w, q, sc, y=y)
+            reps = max(2, 4000 // copies // max(1, wbytes // 2**20 // 8 + 1))
+            t, _ = time_graph(f, reps, 2, 1)
+            us = t * 1e3 / (reps * copies)
+            ent[f"m{m}"] = {"us_per_call": round(us, 3), "weight_gbs": round(wbytes / us / 1e3, 1),
+                            "hbm_frac": round(wbytes / us / 1e3 / peak, 4)}
+        out[name] = ent
+        del ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -326,6 +374,9 @@ def run_ours(args, rank, world, local):
             del stack_layers
             torch.cuda.empty_cache()
 
+    # --- standalone GEMV shapes (tq_gemv; weights rotated past L2 where they fit) ---
+    gemv = {} if args.no_gemv else gemv_sweep(peak)
+
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -361,6 +412,7 @@ def run_ours(args, rank, world, local):
                 "how": "pinned H2D copy + tq_ffn_step + D2H copy per step, graph-replayed",
                 "eager_us_per_step": round(eager_ms * 1e3, 3)},
         "stack": stacks,
+        "gemv": gemv,
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -420,6 +472,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--stack-reps", type=int, default=100)
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-gemv", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many eager steps of the headline workload and exit "
                          "(a small, untimed case for a profiler to capture)")

@@ -108,26 +108,35 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// L2 policy for data read once: its lines are the first evicted, so a
+// stream of them does not push out what other kernels reuse.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // 2D tensor copy global -> shared: the box at (x bytes, y rows) of the tensor
 // described by *tmap (a kernel-parameter tensor map) lands densely at dst;
-// completion is counted in bytes on `bar` (out-of-range parts read as zero).
+// completion is counted in bytes on `bar` (out-of-range parts read as zero);
+// the lines are cached in L2 under `policy`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
 
 // 3D tensor copy global -> shared: the box at (x, y, z) lands densely at dst
-// (x fastest); completion counted in bytes on `bar`.
+// (x fastest); completion counted in bytes on `bar`; L2 policy as above.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -6,13 +6,13 @@
 #include "tq.h"
 #include "tq_kernel.cuh"
 #include "tq_kernel_launch.h"
+#include "tq_kernel_run.cuh"
 #include "tq_tmap.h"
 
 namespace tq {
 
 namespace {
 
-constexpr int kMaxDev = 64;
 constexpr int kPrologueSlots = 16;     // units in flight before the input is staged
 
 struct DevInfo {
@@ -162,48 +162,6 @@ cudaError_t make_mat(MatDesc *md, const WeightRef &w, int fmt) {
     return e;
 }
 
-template <int FMT, int M>
-cudaError_t launch_t(const KArgs &a, const Plan &p, bool coop, cudaStream_t stream) {
-    auto kernel = tq_kernel<FMT, M>;
-    static std::atomic<int> configured[kMaxDev] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= kMaxDev || configured[dev].load() < static_cast<int>(p.bytes)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.bytes));
-        if (e != cudaSuccess) return e;
-        if (dev < kMaxDev) configured[dev].store(static_cast<int>(p.bytes));
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-    if (coop) {
-        // the grid barrier needs every CTA resident at once
-        attr[na].id = cudaLaunchAttributeCooperative;
-        attr[na].val.cooperative = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, kernel, a);
-    if (e != cudaSuccess && coop) {
-        // a driver that refuses the two attributes together: keep the
-        // co-residency guarantee, drop the overlap with the previous launch
-        (void)cudaGetLastError();
-        cfg.attrs = attr + 1;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kernel, a);
-    }
-    return e;
-}
-
 }  // namespace
 
 bool call_fits(const Call &c, cudaError_t *err) {
@@ -266,20 +224,21 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.segready = c.segready;
     a.ticket = c.ticket;
     a.err = c.err;
-    const bool coop = c.do_a && c.do_b;     // phase B waits on other CTAs' rotations
+    if (!c.do_a) return launch_b_only(a, c.fmt, c.m, p.grid, p.bytes, stream);
+    const bool coop = c.do_b;     // phase B waits on other CTAs' rotations
     if (c.fmt == TQ_FMT_TERNARY2) {
         switch (c.m) {
-            case 1: return launch_t<0, 1>(a, p, coop, stream);
-            case 2: return launch_t<0, 2>(a, p, coop, stream);
-            case 3: return launch_t<0, 3>(a, p, coop, stream);
-            default: return launch_t<0, 4>(a, p, coop, stream);
+            case 1: return launch_t<0, 1, false>(a, p.grid, p.bytes, coop, stream);
+            case 2: return launch_t<0, 2, false>(a, p.grid, p.bytes, coop, stream);
+            case 3: return launch_t<0, 3, false>(a, p.grid, p.bytes, coop, stream);
+            default: return launch_t<0, 4, false>(a, p.grid, p.bytes, coop, stream);
         }
     }
     switch (c.m) {
-        case 1: return launch_t<1, 1>(a, p, coop, stream);
-        case 2: return launch_t<1, 2>(a, p, coop, stream);
-        case 3: return launch_t<1, 3>(a, p, coop, stream);
-        default: return launch_t<1, 4>(a, p, coop, stream);
+        case 1: return launch_t<1, 1, false>(a, p.grid, p.bytes, coop, stream);
+        case 2: return launch_t<1, 2, false>(a, p.grid, p.bytes, coop, stream);
+        case 3: return launch_t<1, 3, false>(a, p.grid, p.bytes, coop, stream);
+        default: return launch_t<1, 4, false>(a, p.grid, p.bytes, coop, stream);
     }
 }
 

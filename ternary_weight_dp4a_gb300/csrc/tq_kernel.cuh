@@ -135,9 +135,11 @@ struct KArgs {
 // The tiles and units of one phase for CTA c of G.  Phase A deals in CTA
 // order, phase B in reverse (dealing index G - 1 - c), so the CTAs holding
 // one more phase-B tile are the ones the host gave fewer phase-A tiles.  Unit
-// order: phase A tile-major (tile, matrix, segment); phase B segment-major
-// (segment, tile), so that a CTA needs the segments of h in the order they
-// become ready.
+// order: phase A tile-major (tile, matrix, segment); phase B of a launch that
+// also runs phase A segment-major (segment, tile), so that a CTA needs the
+// segments of h in the order they become ready; a phase-B-only launch
+// (whole input staged up front) tile-major (tile, segment), so that a CTA
+// reads each tile's rows in one pass.
 struct PhaseGeo {
     int n, k, nb, nseg, upt, ntiles, dc, count, units;
     Deal deal;
@@ -659,7 +661,8 @@ __device__ bool stage_segment_b(const KArgs &a, const PhaseGeo &P, int j, uint8_
 }
 
 // Decoded position of a phase's unit: phase A (outer = tile, inner = matrix
-// x segment), phase B (outer = segment, inner = tile); inner runs fastest.
+// x segment), phase B (outer = segment, inner = tile, or tile-major as phase
+// A); inner runs fastest.
 struct UnitPos {
     int outer, inner;
 };
@@ -717,7 +720,10 @@ __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, in
     if (lane == 0) a.hcount[hb] = 0u;
 }
 
-template <int FMT, int M>
+// BO: a launch of phase B alone (a GEMV, or the down projection of a staged
+// h), compiled separately: no phase-A code, the whole input staged up front,
+// units tile-major.
+template <int FMT, int M, bool BO>
 __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxSlots];
@@ -748,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     int *tcnt = reinterpret_cast<int *>(base + a.off_tcnt);
     int *segst = tcnt + 2 * a.tiles_max;
 
-    const PhaseGeo ga = a.do_a ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta, false, a.deal_a) : PhaseGeo{};
+    const PhaseGeo ga = (!BO && a.do_a) ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta, false, a.deal_a) : PhaseGeo{};
     const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta, true, a.deal_b) : PhaseGeo{};
     const int total = ga.units + gb.units;
 
@@ -778,15 +784,19 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             bool ok = true;
             unsigned bad = 0u;
             int k = lane;
-            bool in_a = k < ga.units;
+            bool in_a = !BO && k < ga.units;
+            const int bext = max(BO ? gb.upt : gb.count, 1);   // phase B's inner extent
+            // weights are read once per launch: evict them first, keeping
+            // activations and other kernels' data in L2
+            const uint64_t wpol = l2_policy_evict_first();
             UnitPos u{0, in_a ? k : k - ga.units};
-            unit_advance(u, 0, in_a ? max(ga.upt, 1) : max(gb.count, 1));
+            unit_advance(u, 0, in_a ? max(ga.upt, 1) : bext);
             int slot = k % S, round = k / S;
             for (; k < total && ok; k += kProducerLanes) {
                 if (in_a && k >= ga.units) {
                     in_a = false;
                     u = UnitPos{0, k - ga.units};
-                    unit_advance(u, 0, gb.count);
+                    unit_advance(u, 0, bext);
                 }
                 const PhaseGeo &P = in_a ? ga : gb;
                 int mi, seg, lt;
@@ -795,8 +805,8 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                     mi = u.inner >= P.nseg ? 1 : 0;
                     seg = u.inner - mi * P.nseg;
                 } else {
-                    seg = u.outer;
-                    lt = u.inner;
+                    seg = BO ? u.inner : u.outer;
+                    lt = BO ? u.outer : u.inner;
                     mi = 2;
                 }
                 const int tile = phase_tile(P, G, lt);
@@ -816,18 +826,18 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 const bool sct = md.scales_tma != 0;
                 if (FMT == 0 && md.codes3d) {
                     mbar_arrive_expect_tx(fb, 4096u + (sct ? kScalesSlot : 0u));
-                    tma_load_3d(dst, &md.tm_codes, 0, seg * 2, tile * kTileRows, fb);
+                    tma_load_3d(dst, &md.tm_codes, 0, seg * 2, tile * kTileRows, fb, wpol);
                 } else {
                     const int planes = FMT == 0 ? (seg * kSegBlocks + 4 < P.nb ? 2 : 1) : 1;
                     mbar_arrive_expect_tx(fb, planes * 2048u + (sct ? kScalesSlot : 0u));
                     const int x0 = FMT == 0 ? seg * kSegBlocks * 32 : seg * kSegBlocks * 16;
-                    tma_load_2d(dst, &md.tm_codes, x0, tile * kTileRows, fb);
-                    if (planes == 2) tma_load_2d(dst + 2048, &md.tm_codes, x0 + 128, tile * kTileRows, fb);
+                    tma_load_2d(dst, &md.tm_codes, x0, tile * kTileRows, fb, wpol);
+                    if (planes == 2) tma_load_2d(dst + 2048, &md.tm_codes, x0 + 128, tile * kTileRows, fb, wpol);
                 }
                 if (sct)
                     tma_load_2d(smem_u32(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2)), &md.tm_scales,
-                                seg * kSegBlocks, tile * kTileRows, fb);
-                unit_advance(u, kProducerLanes, in_a ? P.upt : P.count);
+                                seg * kSegBlocks, tile * kTileRows, fb, wpol);
+                unit_advance(u, kProducerLanes, in_a ? P.upt : bext);
                 slot += kProducerLanes;
                 if (slot >= S) {
                     slot -= S;
@@ -857,12 +867,12 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     pdl_wait();
     // A+B launches that rotate h take a launch ticket; its result is needed
     // only in phase B, so it is stored after the input is staged
-    const bool ticketed = a.do_a && a.do_b && a.rotate_h;
+    const bool ticketed = !BO && a.do_a && a.do_b && a.rotate_h;
     unsigned long long ticket = 0;
     if (ticketed && tid == 0) ticket = atomicAdd(a.ticket, 1ull);
 
     // ---- phase A's activation: every CTA rotates + quantises the input
-    if (a.do_a) {
+    if (!BO && a.do_a) {
         const int hidden = ga.k;
         if (a.in_mode == kInRotX) {
             const uint16_t *x = a.x;
@@ -902,6 +912,18 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
         }
         if (ticketed && tid == 0) s_epoch = static_cast<unsigned>(ticket / static_cast<unsigned long long>(G));
         named_barrier(1, kConsumers);
+    } else if (BO) {
+        // ---- a phase-B-only launch: its whole input is in memory already
+        // (the grid-dependency wait above); stage it once, all warps
+        if (a.bst != nullptr) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.bst);
+            uint4 *dst = reinterpret_cast<uint4 *>(act_h);
+            for (int i = tid; i < gb.nb * M * kBlock / 16; i += kConsumers) dst[i] = __ldcg(src + i);
+            for (int i = tid; i < gb.nb * M; i += kConsumers) sn_h[i] = __ldcg(a.bsn + i);
+        } else {
+            stage_plain_range<FMT, M>(a.qb, a.sb, gb.k, 0, gb.nb, act_h, sn_h, warp, kConsumerWarps, lane);
+        }
+        named_barrier(1, kConsumers);
     }
     if (tid == 0) mbar_arrive(smem_u32(&input_bar));
 
@@ -915,7 +937,8 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     float *part_a = part, *part_b = part + static_cast<size_t>(ga.units) * M * kTileRows;
     if (warp < ncw) {
         int kp = 0, slot = 0, round = 0;
-        bool in_a = ga.units > 0;
+        bool in_a = !BO && ga.units > 0;
+        const int bext = max(BO ? gb.upt : gb.count, 1);   // phase B's inner extent
         UnitPos u{0, 0};
         int staged_seg = -1;
         for (;;) {
@@ -926,9 +949,9 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             if (in_a && k >= ga.units) {
                 in_a = false;
                 u = UnitPos{0, 0};
-                unit_advance(u, k - ga.units, gb.count);
+                unit_advance(u, k - ga.units, bext);
             } else {
-                unit_advance(u, k - kp, in_a ? ga.upt : gb.count);
+                unit_advance(u, k - kp, in_a ? ga.upt : bext);
             }
             slot += k - kp;
             while (slot >= S) {
@@ -943,10 +966,10 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
                 mi = u.inner >= P.nseg ? 1 : 0;
                 seg = u.inner - mi * P.nseg;
             } else {
-                seg = u.outer;
-                lt = u.inner;
+                seg = BO ? u.inner : u.outer;
+                lt = BO ? u.outer : u.inner;
                 mi = 2;
-                if (seg != staged_seg) {
+                if (!BO && seg != staged_seg) {
                     if (!stage_segment_b<FMT, M>(a, P, seg, act_h, sn_h, segst, s_epoch, lane)) {
                         ok = false;
                         bad |= 64u;
@@ -1026,13 +1049,14 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
             __threadfence_block();
 
             // ---- the tile's last unit: fold its segment sums with the pairwise
-            // tree and store h (phase A) or y (phase B).  Phase A units of a
-            // tile are consecutive; phase B's are `count` apart.
+            // tree and store h (phase A) or y (phase B).  A tile's units are
+            // consecutive in tile-major order, `count` apart in segment-major.
             const int r = lane >> 4;            // activation rows r, r + 2, ... of the tile's 16 outputs
             const int rr16 = lane & 15;         // output row of the tile
             const int row = tile * kTileRows + rr16;
-            const size_t ustride = static_cast<size_t>(in_a ? 1 : P.count) * M * kTileRows;
-            float *pt = (in_a ? part_a + static_cast<size_t>(lt) * P.upt * M * kTileRows : part_b + static_cast<size_t>(lt) * M * kTileRows) +
+            const bool tmaj = in_a || BO;
+            const size_t ustride = static_cast<size_t>(tmaj ? 1 : P.count) * M * kTileRows;
+            float *pt = (in_a ? part_a : part_b) + static_cast<size_t>(lt) * (tmaj ? P.upt : 1) * M * kTileRows +
                         r * kTileRows + rr16;
             for (int k2 = 0; 2 * k2 < M; ++k2) {
                 const int ra = r + 2 * k2;

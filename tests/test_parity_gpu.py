@@ -59,7 +59,12 @@ def test_rotate_quant_bit_exact(tq, orc, m, k, outliers):
 # GEMV
 # ----------------------------------------------------------------------------
 
-GEMV_SHAPES = [(512, 256), (1000, 384), (77, 1152), (4101, 5120), (96, 17408)]
+# the tiny config, ragged and multi-tile shapes, the FFN's K, and the
+# full-attention projections of the model family the pages describe
+# (head_dim 256, 8:1 GQA with 2 KV heads: q 4096 x 5120, k/v 512 x 5120,
+# o 5120 x 4096)
+GEMV_SHAPES = [(512, 256), (1000, 384), (77, 1152), (4101, 5120), (96, 17408),
+               (4096, 5120), (512, 5120), (5120, 4096)]
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
@@ -82,6 +87,33 @@ def test_gemv_bit_exact(tq, orc, fmt, n, k, m):
     assert np.array_equal(yg.view(np.uint32), y_ref.view(np.uint32))
     y64 = orc.gemv_f64(packed, w.scales, fmt, n, k, q_ref, s_ref)
     assert fold_rel_err(yg, y64, orc, packed, w.scales, fmt, n, k, q_ref, s_ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gemv_wide_shape_sampled_rows(tq, orc, fmt):
+    """A wide GEMV at LM-head scale (N = 131072, K = 5120) in the launch the
+    bench times: 64 sampled output rows against the oracle, which computes
+    them from their own rows of the weights (rows are independent)."""
+    import torch
+    n, k, m = 131072, 5120, 2
+    codes_d, scales_d = synth.weight(n, k, fmt, synth.SEED_TINY_WEIGHT + 17, device="cuda")
+    wdev = tq.pack_weights(codes_d, fmt, scales_d)
+    x = _acts(m, k, 0.01)
+    q_ref, s_ref = orc.rotate_quant(x)
+    q = torch.from_numpy(q_ref).cuda()
+    s = torch.from_numpy(s_ref).cuda()
+    y, dots = tq.gemv(wdev, q, s, blockdots=True)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(5).choice(n - 1, 63, replace=False))
+    rows = np.append(rows, n - 1)                               # the last tile's last row
+    ridx = torch.from_numpy(rows).cuda()
+    sub_codes = codes_d[ridx].cpu().numpy()
+    sub_scales = scales_d[ridx].cpu().numpy()
+    packed = orc.pack(sub_codes, fmt)
+    d_ref = orc.blockdots(packed, fmt, len(rows), k, q_ref)
+    assert np.array_equal(dots.cpu().numpy()[:, rows, :], d_ref)
+    y_ref = orc.gemv(packed, sub_scales, fmt, len(rows), k, q_ref, s_ref)
+    assert np.array_equal(y.cpu().numpy()[:, rows].view(np.uint32), y_ref.view(np.uint32))
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
