@@ -32,12 +32,22 @@
 namespace tq {
 
 constexpr int kConsumerWarps = 15;      // compute warps (warp 15 is the producer)
+constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// Thread count the compiler budgets registers for (the launch uses
+// kThreads): 544 caps 2-bit m = 3, 4 at 96 registers per thread, which
+// measured faster for them than 128 despite a few spills; the rest keep 128.
+template <int FMT, int M>
+constexpr int kBoundThreads = (FMT == 0 && M >= 3) ? kThreads + 32 : kThreads;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kCodesSlot = 4096;        // 16 rows x 8 blocks of codes (2-bit: two 2 KB planes)
 constexpr int kScalesSlot = 256;        // 16 rows x 8 fp16 scales
 constexpr int kMaxSlots = 48;
 constexpr int kMaxRowsPerPass = 4;
+// blocks of a unit per iteration of the unit core's block loop (8: the loop
+// fully unrolled; fewer: a smaller hot loop)
+constexpr int kOneRowBlocksPerIter = 8;
+constexpr int kRowsBlocksPerIter = 4;
 // Producer lanes; lane l issues units k = l (mod kProducerLanes).  The ring
 // has a multiple of kProducerLanes slots, so every fill of a slot comes from
 // one lane, in order: when that lane waits for a slot's previous fill to be
@@ -163,10 +173,6 @@ __host__ __device__ inline PhaseGeo phase_geo(int n, int k, int nmat, int G, int
 
 __device__ __forceinline__ int phase_tile(const PhaseGeo &p, int G, int lt) { return deal_tile(p.deal, G, p.dc, lt); }
 
-// Release/acquire fence at gpu scope (cumulative: orders what this thread
-// has observed, e.g. its warp's stores before a __syncwarp).
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
 // Add with release semantics at gpu scope (fire-and-forget): the writes that
 // precede it (cumulatively) are visible to whoever observes the sum.
 __device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v) {
@@ -178,12 +184,6 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v
     unsigned old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
-}
-
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
@@ -376,8 +376,14 @@ __device__ __forceinline__ void unit_dp4a_1row(const uint8_t *cs, bool codes3d, 
     const int r = lane >> 1, h = lane & 1;
     if (FAST) codes3d = true;
     (void)codes3d;
+    // kOneRowBlocksPerIter blocks per iteration (as unit_dp4a_rows)
+    constexpr int U = kOneRowBlocksPerIter;
+    uint32_t wsq[4] = {wsr[0], wsr[1], wsr[2], wsr[3]};
+#pragma unroll 1
+    for (int bi = 0; bi < kSegBlocks; bi += U) {
 #pragma unroll
-    for (int bl = 0; bl < kSegBlocks; ++bl) {
+    for (int bj = 0; bj < U; ++bj) {
+        const int bl = bi + bj;
         if (!FAST && bl >= bcount) break;
         const int b = b0 + bl;
         int dot[M];
@@ -430,8 +436,8 @@ __device__ __forceinline__ void unit_dp4a_1row(const uint8_t *cs, bool codes3d, 
 #pragma unroll
             for (int mm = 0; mm < M; ++mm) dot[mm] = (part[mm][0] + part[mm][1]) + (part[mm][2] + part[mm][3]);
         }
-        const uint32_t wsw = wsr[bl >> 1];
-        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
+        const uint32_t wsw = wsq[bj >> 1];
+        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bj & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
 #pragma unroll
         for (int mm = 0; mm < M; ++mm) {
             int d = dot[mm] + __shfl_xor_sync(0xffffffffu, dot[mm], 1);
@@ -443,6 +449,9 @@ __device__ __forceinline__ void unit_dp4a_1row(const uint8_t *cs, bool codes3d, 
                 dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
         }
     }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) wsq[t] = t + U / 2 < 4 ? wsq[(t + U / 2) & 3] : 0u;
+    }
 }
 
 template <int FMT, int M, bool FAST>
@@ -452,8 +461,15 @@ __device__ __forceinline__ void unit_dp4a_rows(const uint8_t *cs, bool codes3d, 
     const int r = lane >> 1, h = lane & 1;
     if (FAST) codes3d = true;
     (void)codes3d;
+    // kRowsBlocksPerIter blocks per iteration of a loop that is not
+    // unrolled (a smaller hot loop); the scale words shift down in registers
+    constexpr int U = kRowsBlocksPerIter;
+    uint32_t wsq[4] = {wsr[0], wsr[1], wsr[2], wsr[3]};
+#pragma unroll 1
+    for (int bi = 0; bi < kSegBlocks; bi += U) {
 #pragma unroll
-    for (int bl = 0; bl < kSegBlocks; ++bl) {
+    for (int bj = 0; bj < U; ++bj) {
+        const int bl = bi + bj;
         if (!FAST && bl >= bcount) break;
         const int b = b0 + bl;
         int dot[M];
@@ -525,8 +541,8 @@ __device__ __forceinline__ void unit_dp4a_rows(const uint8_t *cs, bool codes3d, 
 #pragma unroll
             for (int mm = 0; mm < M; ++mm) dot[mm] = (part[mm][0] + part[mm][1]) + (part[mm][2] + part[mm][3]);
         }
-        const uint32_t wsw = wsr[bl >> 1];
-        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
+        const uint32_t wsw = wsq[bj >> 1];
+        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bj & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
 #pragma unroll
         for (int mm = 0; mm < M; ++mm) {
             const int d = dot[mm] + __shfl_xor_sync(0xffffffffu, dot[mm], 1);
@@ -537,6 +553,9 @@ __device__ __forceinline__ void unit_dp4a_rows(const uint8_t *cs, bool codes3d, 
             if (!FAST && dots != nullptr && h == 0 && row < n)
                 dots[(static_cast<size_t>(mm) * n + row) * nb + b] = __float2int_rn(v);
         }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) wsq[t] = t + U / 2 < 4 ? wsq[(t + U / 2) & 3] : 0u;
     }
 }
 
@@ -724,7 +743,7 @@ __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, in
 // h), compiled separately: no phase-A code, the whole input staged up front,
 // units tile-major.
 template <int FMT, int M, bool BO>
-__global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxSlots];
     __shared__ __align__(8) uint64_t empty_bar[kMaxSlots];
@@ -772,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1) tq_kernel(const __grid_constant__
     __syncthreads();
     pdl_launch_dependents();
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         // Lanes 0..kProducerLanes-1 each issue every kProducerLanes-th unit,
         // so several units are in the issue pipe at once; unit positions and
