@@ -21,12 +21,14 @@ FMT_BINARY1 = 1
 BLOCK = 128
 MAX_ROWS = 8
 
-# every entry point include/tq.h declares
+# every entry point include/tq.h and include/tq_lifecycle.h declare
 EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",
            "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_workspace_init",
            "tq_ffn_step", "tq_ffn_stage_input", "tq_ffn_stage_gateup", "tq_ffn_stage_down",
            "tq_ffn_stack", "tq_ffn_static_workspace_bytes", "tq_ffn_step_static",
-           "tq_rmsnorm_bf16")
+           "tq_rmsnorm_bf16",
+           "tq_lifecycle_init", "tq_lifecycle_load", "tq_lifecycle_copy", "tq_lifecycle_alloc",
+           "tq_lifecycle_free", "tq_lifecycle_poll", "tq_lifecycle_release", "tq_lifecycle_destroy")
 
 _lock = threading.Lock()
 _lib = None
@@ -44,6 +46,31 @@ class TQError(RuntimeError):
 class _Weight(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("n", ctypes.c_int32), ("k", ctypes.c_int32), ("fmt", ctypes.c_int32)]
+
+
+# tq_lifecycle.h
+_LC_ALLOC = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32)
+_LC_RELEASE = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32)
+_LC_FREE_BYTES = ctypes.CFUNCTYPE(ctypes.c_size_t, ctypes.c_void_p)
+_LC_BUILD = ctypes.CFUNCTYPE(ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t)
+
+
+class _LcHooks(ctypes.Structure):
+    _fields_ = [("alloc", _LC_ALLOC), ("release", _LC_RELEASE), ("free_bytes", _LC_FREE_BYTES),
+                ("build", _LC_BUILD), ("ctx", ctypes.c_void_p)]
+
+
+class _LcConfig(ctypes.Structure):
+    _fields_ = [("copy_bytes", ctypes.c_size_t), ("reserve_bytes", ctypes.c_size_t),
+                ("rebuild_margin", ctypes.c_size_t), ("rebuild_after", ctypes.c_int32)]
+
+
+class _Lifecycle(ctypes.Structure):
+    _fields_ = [("cfg", _LcConfig), ("hooks", _LcHooks), ("copy", ctypes.c_void_p),
+                ("state", ctypes.c_int32), ("polls_since_change", ctypes.c_int32),
+                ("builds", ctypes.c_int64), ("rebuilds", ctypes.c_int64), ("releases", ctypes.c_int64),
+                ("alloc_failures", ctypes.c_int64), ("retries_ok", ctypes.c_int64),
+                ("build_failures", ctypes.c_int64)]
 
 
 def load():
@@ -78,9 +105,24 @@ def load():
             L.tq_ffn_static_workspace_bytes.argtypes = []
             L.tq_ffn_static_workspace_bytes.restype = sz
             L.tq_ffn_step_static.argtypes = [W, W, W, vp, i32, vp, vp]
+            LC = ctypes.POINTER(_Lifecycle)
+            L.tq_lifecycle_init.argtypes = [LC, ctypes.POINTER(_LcConfig), ctypes.POINTER(_LcHooks)]
+            L.tq_lifecycle_load.argtypes = [LC]
+            L.tq_lifecycle_copy.argtypes = [LC]
+            L.tq_lifecycle_copy.restype = vp
+            L.tq_lifecycle_alloc.argtypes = [LC, sz, i32]
+            L.tq_lifecycle_alloc.restype = vp
+            L.tq_lifecycle_free.argtypes = [LC, vp, sz, i32]
+            L.tq_lifecycle_free.restype = None
+            L.tq_lifecycle_poll.argtypes = [LC]
+            L.tq_lifecycle_release.argtypes = [LC]
+            L.tq_lifecycle_release.restype = None
+            L.tq_lifecycle_destroy.argtypes = [LC]
+            L.tq_lifecycle_destroy.restype = None
             for name in EXPORTS:
                 if name not in ("tq_status_string", "tq_last_cuda_error", "tq_ffn_workspace_bytes",
-                                "tq_ffn_static_workspace_bytes"):
+                                "tq_ffn_static_workspace_bytes", "tq_lifecycle_copy", "tq_lifecycle_alloc",
+                                "tq_lifecycle_free", "tq_lifecycle_release", "tq_lifecycle_destroy"):
                     getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -261,3 +303,128 @@ def rmsnorm_bf16(y, eps: float = 1e-6, x_out=None, stream=None):
     _check("tq_rmsnorm_bf16", load().tq_rmsnorm_bf16(_ptr(y), m, n, eps, _ptr(x_out),
                                                      _stream(stream)))
     return x_out
+
+
+# ---------------------------------------------------------------------------
+# lifecycle of the ternary weight copy (include/tq_lifecycle.h)
+# ---------------------------------------------------------------------------
+
+class CopyLifecycle:
+    """The host-side policy of include/tq_lifecycle.h around a caller's hooks.
+
+    ``hooks`` has ``alloc(nbytes, purpose) -> address or 0``,
+    ``release(address, nbytes, purpose)``, ``free_bytes() -> int`` and
+    ``build(address, nbytes) -> bool``; the policy itself runs in libtq.
+    A hook that raises counts as a failure (alloc/build) or as 0 free bytes.
+    """
+
+    STATES = ("absent", "resident", "skipped", "released", "failed")
+    COPY, OTHER = 0, 1
+
+    def __init__(self, copy_bytes: int, reserve_bytes: int, hooks, rebuild_margin: int = 0,
+                 rebuild_after: int = 0):
+        L = load()
+
+        def _alloc(_ctx, nbytes, purpose):
+            try:
+                return hooks.alloc(int(nbytes), int(purpose)) or None
+            except Exception:
+                return None
+
+        def _release(_ctx, ptr, nbytes, purpose):
+            try:
+                hooks.release(int(ptr or 0), int(nbytes), int(purpose))
+            except Exception:
+                pass
+
+        def _free_bytes(_ctx):
+            try:
+                return max(0, int(hooks.free_bytes()))
+            except Exception:
+                return 0
+
+        def _build(_ctx, ptr, nbytes):
+            try:
+                return 0 if hooks.build(int(ptr or 0), int(nbytes)) else 1
+            except Exception:
+                return 1
+
+        # the callbacks must outlive the struct that points at them
+        self._cbs = (_LC_ALLOC(_alloc), _LC_RELEASE(_release), _LC_FREE_BYTES(_free_bytes),
+                     _LC_BUILD(_build))
+        self._hooks = _LcHooks(*self._cbs, None)
+        self._cfg = _LcConfig(copy_bytes, reserve_bytes, rebuild_margin, rebuild_after)
+        self._lc = _Lifecycle()
+        _check("tq_lifecycle_init",
+               L.tq_lifecycle_init(ctypes.byref(self._lc), ctypes.byref(self._cfg),
+                                   ctypes.byref(self._hooks)))
+
+    def load(self) -> str:
+        _check("tq_lifecycle_load", load().tq_lifecycle_load(ctypes.byref(self._lc)))
+        return self.state
+
+    @property
+    def copy(self):
+        """Address of the resident copy, or None."""
+        return load().tq_lifecycle_copy(ctypes.byref(self._lc))
+
+    def alloc(self, nbytes: int, purpose: int = OTHER):
+        """Memory for other work; releases the copy and retries once on failure."""
+        return load().tq_lifecycle_alloc(ctypes.byref(self._lc), nbytes, purpose)
+
+    def free(self, ptr, nbytes: int, purpose: int = OTHER) -> None:
+        load().tq_lifecycle_free(ctypes.byref(self._lc), ptr, nbytes, purpose)
+
+    def poll(self) -> str:
+        _check("tq_lifecycle_poll", load().tq_lifecycle_poll(ctypes.byref(self._lc)))
+        return self.state
+
+    def release(self) -> None:
+        load().tq_lifecycle_release(ctypes.byref(self._lc))
+
+    def destroy(self) -> None:
+        load().tq_lifecycle_destroy(ctypes.byref(self._lc))
+
+    @property
+    def state(self) -> str:
+        return self.STATES[self._lc.state]
+
+    def counters(self) -> dict:
+        return {k: int(getattr(self._lc, k)) for k in
+                ("builds", "rebuilds", "releases", "alloc_failures", "retries_ok", "build_failures")}
+
+
+class TorchDeviceHooks:
+    """Lifecycle hooks over PyTorch's CUDA allocator.  ``build_fn(tensor)``
+    fills a uint8 tensor of the copy's size (e.g. packs weights into it) and
+    returns True on success.  Free memory counts the driver's free bytes plus
+    what PyTorch holds cached but unused."""
+
+    def __init__(self, build_fn, device="cuda"):
+        self.build_fn = build_fn
+        self.device = device
+        self._live = {}
+
+    def alloc(self, nbytes, purpose):
+        import torch
+        try:
+            t = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        except torch.cuda.OutOfMemoryError:
+            return 0
+        self._live[t.data_ptr()] = t
+        return t.data_ptr()
+
+    def release(self, ptr, nbytes, purpose):
+        self._live.pop(ptr, None)
+
+    def free_bytes(self):
+        import torch
+        free, _total = torch.cuda.mem_get_info(self.device)
+        return free + torch.cuda.memory_reserved(self.device) - torch.cuda.memory_allocated(self.device)
+
+    def build(self, ptr, nbytes):
+        return bool(self.build_fn(self._live[ptr]))
+
+    def tensor(self, ptr):
+        """The tensor behind an address alloc returned (None once released)."""
+        return self._live.get(ptr)

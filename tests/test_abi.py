@@ -1,4 +1,4 @@
-"""The C-ABI library loads and exports every entry point include/tq.h declares,
+"""The C-ABI library loads and exports every entry point include/*.h declare,
 and rejects bad arguments before touching the GPU.  No GPU needed."""
 import ctypes
 import os
@@ -19,9 +19,15 @@ def lib():
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "tq.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        # function declarations only (not the hook members "(*name)(")
+        names |= set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_and_binding_agree():
