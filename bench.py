@@ -442,6 +442,23 @@ def profile_steps(n: int):
     torch.cuda.synchronize()
 
 
+def profile_gemv(n: int):
+    """n eager m = 1 tq_gemv calls on the 17408 x 5120 gate shape, rotating
+    over the weight sets' gate matrices (no timing, no JSON line)."""
+    import torch
+    from ternary_weight_dp4a_gb300 import build as tqbuild
+    from ternary_weight_dp4a_gb300 import synth, tq
+    tqbuild.build()
+    tq.load()
+    layers = make_weights(tq.FMT_TERNARY2, N_SETS, HIDDEN, INTER)
+    x = synth.activation(1, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
+    q, s = tq.rotate_quant(x)
+    y = torch.empty((1, INTER), dtype=torch.float32, device="cuda")
+    for i in range(n):
+        tq.gemv(layers[i % N_SETS][0], q, s, y=y)
+    torch.cuda.synchronize()
+
+
 def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1):
     """Time the oracle's FFN step on the host cores on a bounded sample: as many
     full layer steps (m rows) as fit in about ``budget_s`` seconds."""
@@ -482,6 +499,8 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many eager steps of the headline workload and exit "
                          "(a small, untimed case for a profiler to capture)")
+    ap.add_argument("--profile-gemv", type=int, default=0,
+                    help="run this many eager m = 1 GEMVs on the 17408 x 5120 gate shape and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -509,6 +528,9 @@ def main():
     rank, world, local = dist_setup()
     if args.profile_steps > 0:
         profile_steps(args.profile_steps)
+        return
+    if args.profile_gemv > 0:
+        profile_gemv(args.profile_gemv)
         return
     result = run_ours(args, rank, world, local)
     if rank == 0:
