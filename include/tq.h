@@ -129,6 +129,20 @@ tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t
 /* Bytes of device workspace tq_ffn_step / tq_ffn_stack need for these sizes. */
 size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter);
 
+/* Byte offset in such a workspace of its error word (uint32, 4-byte aligned;
+ * 0 for invalid sizes).  Every wait inside the FFN kernels is bounded (about
+ * 0.5 s of GPU clock cycles); a wait that runs out ORs a bit into this word
+ * and the kernel finishes without hanging, its outputs undefined:
+ *   bit 0  the weight stream waited for a free ring slot
+ *   bit 1  the weight stream waited for its last copies to land
+ *   bit 2  a compute warp waited for a slot's weights
+ *   bit 3  a compute warp waited for its unit to be issued
+ *   bit 4  the weight stream waited for the input to be staged
+ *   bit 6  the down phase waited for a 1024-wide segment of h to be rotated
+ * The word stays set until tq_ffn_workspace_init; read it (4 bytes) after
+ * synchronising the stream. */
+size_t tq_ffn_workspace_error_offset(int32_t m, int32_t hidden, int32_t inter);
+
 /* Zero-fill a workspace (an async memset on `stream`).  A workspace must be
  * zero-filled once before its first use; every FFN call leaves it reusable.
  * After a call that failed in flight (a CUDA error surfaced at

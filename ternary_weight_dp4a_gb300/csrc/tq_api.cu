@@ -279,6 +279,11 @@ size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter) {
     return ffn_layout(m, hidden, inter).total;
 }
 
+size_t tq_ffn_workspace_error_offset(int32_t m, int32_t hidden, int32_t inter) {
+    if (m < 1 || hidden < 1 || inter < 1) return 0;
+    return ffn_layout(m, hidden, inter).err;
+}
+
 tq_status tq_ffn_workspace_init(void *workspace, size_t workspace_bytes, tq_stream_t stream) {
     if (workspace == nullptr) return TQ_ERR_INVALID_ARG;
     return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes,

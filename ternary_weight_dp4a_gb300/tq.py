@@ -23,7 +23,8 @@ MAX_ROWS = 8
 
 # every entry point include/tq.h and include/tq_lifecycle.h declare
 EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",
-           "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_workspace_init",
+           "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_workspace_error_offset",
+           "tq_ffn_workspace_init",
            "tq_ffn_step", "tq_ffn_stage_input", "tq_ffn_stage_gateup", "tq_ffn_stage_down",
            "tq_ffn_stack", "tq_ffn_static_workspace_bytes", "tq_ffn_step_static",
            "tq_rmsnorm_bf16",
@@ -95,6 +96,8 @@ def load():
             L.tq_ffn_gateup.argtypes = [W, W, vp, vp, i32, vp, vp]
             L.tq_ffn_workspace_bytes.argtypes = [i32, i32, i32]
             L.tq_ffn_workspace_bytes.restype = sz
+            L.tq_ffn_workspace_error_offset.argtypes = [i32, i32, i32]
+            L.tq_ffn_workspace_error_offset.restype = sz
             L.tq_ffn_workspace_init.argtypes = [vp, sz, vp]
             L.tq_ffn_step.argtypes = [W, W, W, vp, i32, vp, vp, sz, vp]
             L.tq_ffn_stage_input.argtypes = [vp, i32, i32, i32, vp, sz, vp]
@@ -121,7 +124,7 @@ def load():
             L.tq_lifecycle_destroy.restype = None
             for name in EXPORTS:
                 if name not in ("tq_status_string", "tq_last_cuda_error", "tq_ffn_workspace_bytes",
-                                "tq_ffn_static_workspace_bytes", "tq_lifecycle_copy", "tq_lifecycle_alloc",
+                                "tq_ffn_workspace_error_offset", "tq_ffn_static_workspace_bytes", "tq_lifecycle_copy", "tq_lifecycle_alloc",
                                 "tq_lifecycle_free", "tq_lifecycle_release", "tq_lifecycle_destroy"):
                     getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -227,6 +230,13 @@ def ffn_workspace(m: int, hidden: int, inter: int, device="cuda"):
 def ffn_workspace_init(workspace, stream=None):
     _check("tq_ffn_workspace_init", load().tq_ffn_workspace_init(
         _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def ffn_workspace_error(workspace, m: int, hidden: int, inter: int) -> int:
+    """The workspace's error word (bits of the waits that ran out; see
+    tq_ffn_workspace_error_offset).  Reads 4 bytes back, so it synchronises."""
+    off = load().tq_ffn_workspace_error_offset(m, hidden, inter)
+    return int(workspace[off:off + 4].cpu().numpy().view("<u4")[0])
 
 
 def ffn_stage_input(x, inter: int, workspace, stream=None):

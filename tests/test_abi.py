@@ -54,6 +54,15 @@ def test_workspace_bytes(lib):
     assert lib.tq_ffn_workspace_bytes(0, 5120, 17408) == 0
 
 
+def test_workspace_error_offset(lib):
+    from _util import ws_offsets
+    for m, hidden, inter in ((1, 5120, 17408), (8, 5120, 17408), (3, 256, 512)):
+        off = lib.tq_ffn_workspace_error_offset(m, hidden, inter)
+        assert off == ws_offsets(m, hidden, inter)["err"]
+        assert off % 4 == 0 and off + 4 <= lib.tq_ffn_workspace_bytes(m, hidden, inter)
+    assert lib.tq_ffn_workspace_error_offset(1, 0, 512) == 0
+
+
 def _w(codes=0x1000, scales=0x2000, n=512, k=256, fmt=0):
     return tq._Weight(codes, scales, n, k, fmt)
 

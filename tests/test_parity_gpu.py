@@ -274,6 +274,35 @@ def test_ffn_repeat_runs_bit_identical(tq):
         assert np.array_equal(again.view(np.uint32), first.view(np.uint32))
 
 
+def test_ffn_wait_that_runs_out_sets_error_and_workspace_recovers(tq, orc):
+    """Failure detection without a fault: the workspace's launch ticket is set
+    1000 launches ahead, so the count the down phase waits for on every
+    segment of h is one that no launch reaches.  Each such wait is bounded
+    (about 0.5 s): the kernel finishes, the error word carries bit 6, the
+    context stays usable, and after tq_ffn_workspace_init the same step is
+    bit-exact against the oracle again."""
+    import torch
+    hidden, inter, m = 256, 2048, 1
+    mats = ffn_mats(hidden, inter, 0)
+    g, u, d = mats
+    x = _acts(m, hidden, 0.01)
+    ws = tq.ffn_workspace(m, hidden, inter)
+    o = ws_offsets(m, hidden, inter)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ticket = np.array([1000 * sms], dtype=np.uint64).view(np.uint8)
+    ws[o["sync"]:o["sync"] + 8].copy_(torch.from_numpy(ticket).cuda())
+    tq.ffn_step(g.dev, u.dev, d.dev, bf16_tensor(x), workspace=ws)
+    torch.cuda.synchronize()
+    err = tq.ffn_workspace_error(ws, m, hidden, inter)
+    assert err & 64, hex(err)
+    tq.ffn_workspace_init(ws)
+    y = tq.ffn_step(g.dev, u.dev, d.dev, bf16_tensor(x), workspace=ws)
+    torch.cuda.synchronize()
+    assert tq.ffn_workspace_error(ws, m, hidden, inter) == 0
+    ref = _ffn_orc(orc, mats, x)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), ref["y"].view(np.uint32))
+
+
 def test_ffn_zero_activation(tq):
     import torch
     mats = ffn_mats(256, 512, 0)
