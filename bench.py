@@ -36,6 +36,29 @@ WORKLOAD = "ffn_layer_h5120_i17408_ternary2"
 BLOCK = 128
 
 
+NOMINAL_HBM_GBS = 8000.0     # the nominal GB300 HBM3e figure the scope's roofline quotes
+SMS = 152
+INT_LANES_PER_CLK = 64       # integer pipe (prmt, lop3, shf, dp4a) per SM and clock, measured
+
+
+def int_ops_per_weight(fmt: int, rows: int) -> float:
+    """Integer-pipe ops per weight in one pass of ``rows`` <= 4 activation rows,
+    counting only the decode and the dot products: 2-bit, 7 ops (3 shifts, 4
+    prmt) per 16 weights plus one dp4a per 4 weights and row; 1-bit, a shift
+    and a mask per 4 weights plus one dp4a per 4 weights and row."""
+    return (7 + 4 * rows) / 16 if fmt == 0 else (2 + rows) / 4
+
+
+def alu_bound_us(fmt: int, m: int, weights: int, sm_mhz: float) -> float:
+    """Time the integer pipe needs for ``weights`` weights at m rows (passes of
+    at most 4 rows, each decoding every weight again) on every SM at
+    ``sm_mhz``: a lower bound on a dp4a step, beside the HBM bound."""
+    ops = 0.0
+    for r0 in range(0, m, 4):
+        ops += int_ops_per_weight(fmt, min(4, m - r0))
+    return weights * ops / (SMS * INT_LANES_PER_CLK * sm_mhz * 1e6) * 1e6
+
+
 def layer_bytes(hidden: int, inter: int, fmt: int) -> int:
     """Algorithmic bytes of one FFN layer: packed codes + fp16 scales of gate, up, down."""
     per = 4 if fmt == 0 else 8
@@ -306,6 +329,9 @@ def run_ours(args, rank, world, local):
     ms = max_over_ranks(ms, world)
     ms_step = ms / steps
     value = world * lb / (ms_step * 1e-3) / 1e9
+    # the integer-pipe bound uses the SM clock sampled under load (max clock if none)
+    sm_mhz = float((clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0)
+    layer_w = 3 * HIDDEN * INTER
 
     # --- batch sweep m = 1, 2, 4, 8 (same weights, packed rows) ---
     sweep = {}
@@ -316,7 +342,9 @@ def run_ours(args, rank, world, local):
         us = t * 1e3 / (sweep_reps * N_SETS)
         sweep[f"m{m}"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
                           "tokens_per_s": round(m * 1e6 / us, 1),
-                          "hbm_frac": round(lb / us / 1e3 / peak, 4)}
+                          "hbm_frac": round(lb / us / 1e3 / peak, 4),
+                          "alu_bound_us": round(alu_bound_us(0, m, layer_w, sm_mhz), 3)}
+        sweep[f"m{m}"]["alu_frac"] = round(sweep[f"m{m}"]["alu_bound_us"] / us, 4)
 
     # --- roofline: at m = 1 the step is one launch of the persistent step
     #     kernel (tq_kernel<0,1>: gate/up, SiLU*up, rotation of h, down), so the
@@ -373,10 +401,12 @@ def run_ours(args, rank, world, local):
                                   args.stack_reps, 2, world)
                 t = max_over_ranks(t, world)
                 us = t * 1e3 / args.stack_reps
+                alu = alu_bound_us(sfmt, m, 64 * layer_w, sm_mhz)
                 stacks[f"{'ternary2' if sfmt == 0 else 'binary1'}_64L_m{m}"] = {
                     "us_per_token_step": round(us, 2), "bytes_per_step": sb,
                     "weight_gbs": round(sb / us / 1e3, 1), "hbm_frac": round(sb / us / 1e3 / peak, 4),
-                    "tokens_per_s": round(m * 1e6 / us, 1)}
+                    "tokens_per_s": round(m * 1e6 / us, 1),
+                    "alu_bound_us": round(alu, 2), "alu_frac": round(alu / us, 4)}
             del stack_layers
             torch.cuda.empty_cache()
 
@@ -409,6 +439,9 @@ def run_ours(args, rank, world, local):
                      "kernel": "tq_kernel<0,1> (whole FFN step: gate/up + SiLU*up + h rotation + down)",
                      "achieved": round(k_achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(k_achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal": round(k_achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "alu_bound_us": round(alu_bound_us(0, 1, layer_w, sm_mhz), 3),
                      "bytes_per_launch": lb, "avg_launch_us": round(k_us, 3),
                      "launches_timed": launches,
                      "traffic": recorded_traffic("step_m1")},
@@ -459,31 +492,110 @@ def profile_gemv(n: int):
     torch.cuda.synchronize()
 
 
-def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1):
+def host_info() -> dict:
+    """Core count and CPU model of this host, read at run time."""
+    import platform
+    import subprocess
+    model = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            key, _, val = line.partition(":")
+            if key.strip().lower() in ("model name", "cpu model"):
+                model = val.strip()
+                break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
+def _time_calls(fn, budget_s: float):
+    """Seconds per call of fn over about budget_s seconds (at least one call)."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / n * (n + 1) > 2 * budget_s:
+            return el / n, n
+
+
+def _ffn_mats_host(fmt: int, layer: int = 0):
+    from oracle import oracle
+    from ternary_weight_dp4a_gb300 import synth
+    mats = []
+    for j, (n, k) in enumerate([(INTER, HIDDEN), (INTER, HIDDEN), (HIDDEN, INTER)]):
+        codes, scales = synth.weight(n, k, fmt, synth.ffn_weight_seed(layer, j))
+        mats.extend([oracle.pack(codes, fmt), scales])
+        del codes
+    return mats
+
+
+def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1, extras: bool = False):
     """Time the oracle's FFN step on the host cores on a bounded sample: as many
-    full layer steps (m rows) as fit in about ``budget_s`` seconds."""
+    full layer steps (m rows) as fit in about ``budget_s`` seconds.  With
+    ``extras`` also: the same step on 1 and on cores - 2 threads, the tiny GEMV,
+    and per-token estimates of the 64-layer stacks from a sample of layers."""
     from oracle import oracle
     from ternary_weight_dp4a_gb300 import synth
     oracle.build()
-    mats = []
-    for j, (n, k) in enumerate([(INTER, HIDDEN), (INTER, HIDDEN), (HIDDEN, INTER)]):
-        codes, scales = synth.weight(n, k, fmt, synth.ffn_weight_seed(0, j))
-        mats.extend([oracle.pack(codes, fmt), scales])
-        del codes
+    mats = _ffn_mats_host(fmt)
     x = synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01)
     lb = layer_bytes(HIDDEN, INTER, fmt)
-    steps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.ffn_step(*mats, fmt, HIDDEN, INTER, x)
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or el / steps * (steps + 1) > 2 * budget_s:
-            break
-    return {"value": round(lb * steps / el / 1e9, 4), "unit": "GB/s",
-            "cores": oracle.get_threads(), "kind": "oracle",
-            "sample": f"{steps} full FFN layer step(s), m={m}, hidden {HIDDEN}, "
-                      f"intermediate {INTER}, 2-bit; {el:.1f} s",
-            "us_per_step": round(el / steps * 1e6, 1)}
+    threads = oracle.get_threads()
+    sec, steps = _time_calls(lambda: oracle.ffn_step(*mats, fmt, HIDDEN, INTER, x), budget_s)
+    out = {"value": round(lb / sec / 1e9, 4), "unit": "GB/s",
+           "cores": threads, "kind": "oracle",
+           "sample": f"{steps} full FFN layer step(s), m={m}, hidden {HIDDEN}, "
+                     f"intermediate {INTER}, 2-bit; {sec * steps:.1f} s",
+           "us_per_step": round(sec * 1e6, 1)}
+    if not extras:
+        return out
+    out["host"] = host_info()
+    # the same step on 1 thread, cores - 2 threads (cores left to the OS) and all
+    scan = []
+    for t in sorted({1, max(1, threads - 2), threads}):
+        oracle.set_threads(t)
+        st, n = _time_calls(lambda: oracle.ffn_step(*mats, fmt, HIDDEN, INTER, x),
+                            min(3.0, budget_s / 3))
+        scan.append({"threads": t, "us_per_step": round(st * 1e6, 1),
+                     "weight_gbs": round(lb / st / 1e9, 4), "steps": n})
+    oracle.set_threads(threads)
+    out["threads_scan"] = scan
+    configs = {}
+    # tiny GEMV, K = 256, N = 512 (2-bit)
+    codes, scales = synth.weight(512, 256, 0, synth.SEED_TINY_WEIGHT)
+    packed = oracle.pack(codes, 0)
+    q, s = oracle.rotate_quant(synth.activation(1, 256, synth.SEED_ACT_BASE, 0.0))
+    st, n = _time_calls(lambda: oracle.gemv(packed, scales, 0, 512, 256, q, s), 0.5)
+    tb = 512 * 256 // 4 + 2 * 512 * 2
+    configs["tiny_gemv_n512_k256"] = {"us_per_call": round(st * 1e6, 2), "weight_gbs": round(tb / st / 1e9, 4),
+                                      "sample": f"{n} calls"}
+    # 64-layer stacks: one layer (step + RMS-normalise) timed, times 64
+    for sfmt, ms in ((0, (1,)), (1, (1, 2, 4, 8))):
+        smats = mats if sfmt == fmt else _ffn_mats_host(sfmt)
+        for mm in ms:
+            xm = synth.activation(mm, HIDDEN, synth.SEED_ACT_BASE, 0.01)
+
+            def layer():
+                y = oracle.ffn_step(*smats, sfmt, HIDDEN, INTER, xm)["y"]
+                oracle.rmsnorm_bf16(y, 1e-6)
+            st, n = _time_calls(layer, 0.5)
+            sb = 64 * layer_bytes(HIDDEN, INTER, sfmt)
+            configs[f"{'ternary2' if sfmt == 0 else 'binary1'}_64L_m{mm}"] = {
+                "us_per_token_step": round(64 * st * 1e6, 1), "weight_gbs": round(sb / (64 * st) / 1e9, 4),
+                "sample": f"{n} layer(s) timed, x 64"}
+        del smats
+    out["configs"] = configs
+    return out
 
 
 def main():
@@ -534,7 +646,7 @@ def main():
         return
     result = run_ours(args, rank, world, local)
     if rank == 0:
-        result["cpu_baseline"] = cpu_oracle_baseline(args.cpu_budget)
+        result["cpu_baseline"] = cpu_oracle_baseline(args.cpu_budget, extras=True)
         print(json.dumps(result))
     if world > 1:
         import torch.distributed as dist
