@@ -436,7 +436,7 @@ def run_ours(args, rank, world, local):
         "hbm_frac": round(value / world / peak, 4),
         "sweep": sweep,
         "roofline": {"bound": "hbm",
-                     "kernel": "tq_kernel<0,1> (whole FFN step: gate/up + SiLU*up + h rotation + down)",
+                     "kernel": "tq_kernel<0,1,false> (whole FFN step: gate/up + SiLU*up + h rotation + down)",
                      "achieved": round(k_achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(k_achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal": round(k_achieved / NOMINAL_HBM_GBS, 4),
