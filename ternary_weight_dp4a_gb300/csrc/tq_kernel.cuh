@@ -13,10 +13,11 @@
 // pairwise tree and runs the tile's epilogue.
 //
 // Phase A (gate/up): input x rotated + quantised by every CTA (or read as
-// int8), units of gate and up, epilogue h = bf16(silu(g) * u); the CTA whose
+// int8), units of gate and up, epilogue h = bf16(silu(g) * u); the warp whose
 // tile completes a 128-block of h rotates and quantises that block.
-// Phase B (down, or a plain GEMV): input int8 rows staged from global memory,
-// epilogue y (fp32), optionally the int32 block dots.
+// Phase B (down, or a plain GEMV): input int8 rows staged from global memory
+// (a segment at a time as h becomes ready, or all at once in a launch of
+// phase B alone), epilogue y (fp32), optionally the int32 block dots.
 // A step runs A and B in one launch without a grid barrier: a phase-B unit
 // waits only until the 8 blocks of h its segment reads are rotated.  The
 // producer never waits for the consumers' phases: weights do not depend on
@@ -139,7 +140,7 @@ struct KArgs {
     unsigned long long *ticket;
     unsigned *err;            // wait that ran out: bit 0 producer (slot free), 1 producer drain,
                               // 2 consumer (slot data), 3 consumer (slot issued), 4 producer
-                              // (input staged), 5 epilogue (tile folded), 6 phase B (segment of h)
+                              // (input staged), 6 phase B (segment of h); bit 5 is unused
 };
 
 // The tiles and units of one phase for CTA c of G.  Phase A deals in CTA
