@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 HIDDEN, INTER = 5120, 17408
 N_SETS = 8
+SWEEP_ROWS = (1, 2, 4, 8, 16, 32, 64)
 METRIC = "ternary FFN decode step: weight GB/s & % HBM roofline, µs/token at batch 1/2/4/8"
 WORKLOAD = "ffn_layer_h5120_i17408_ternary2"
 BLOCK = 128
@@ -311,7 +312,7 @@ def run_ours(args, rank, world, local):
     lb = layer_bytes(HIDDEN, INTER, fmt)
     layers = make_weights(fmt, N_SETS, HIDDEN, INTER)
     xs = {m: synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
-          for m in (1, 2, 4, 8)}
+          for m in SWEEP_ROWS}
     ys = {m: torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda") for m in xs}
     wss = {m: tq.ffn_workspace(m, HIDDEN, INTER) for m in xs}
 
@@ -333,10 +334,13 @@ def run_ours(args, rank, world, local):
     sm_mhz = float((clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0)
     layer_w = 3 * HIDDEN * INTER
 
-    # --- batch sweep m = 1, 2, 4, 8 (same weights, packed rows) ---
+    # --- batch sweep: packed decode steps m = 1, 2, 4, 8, and verify-sized
+    #     blocks m = 16, 32, 64 (passes of at most 4 rows; same weights) ---
     sweep = {}
-    sweep_reps = max(1, min(reps, 2000 // N_SETS))
-    for m in (1, 2, 4, 8):
+    for m in SWEEP_ROWS:
+        # about 2000 steps' worth of weight streams per m (fewer graph replays
+        # for the multi-pass blocks)
+        sweep_reps = max(1, min(reps, 2000 // N_SETS // max(1, m // 8)))
         t, _ = time_graph(one_pass(m), sweep_reps, 2, world)
         t = max_over_ranks(t, world)
         us = t * 1e3 / (sweep_reps * N_SETS)

@@ -21,7 +21,10 @@
  *     Errors raised later by kernels in flight surface at the caller's next
  *     synchronisation, as for any CUDA call.
  *   - Outputs must not overlap inputs or each other.
- *   - Sizes: k and hidden/intermediate are multiples of 128; 1 <= m <= 8.
+ *   - Sizes: k and hidden/intermediate are multiples of 128; 1 <= m <= 64.
+ *     Rows run in passes of at most 4 through one weight stream each: up to
+ *     8 rows is the packed decode step; 9..64 rows (verify or prefill blocks)
+ *     run the same passes, each re-reading the weights.
  *   - Floating point is IEEE binary32 with the rounding of each step
  *     documented at the entry point; results do not depend on m, on the
  *     stream or on how many SMs the GPU has.
@@ -69,11 +72,11 @@ typedef struct {
     int32_t fmt; /* tq_format */
 } tq_weight;
 
-/* Most activation rows in one packed step.  The GEMV also needs
- * m * (k/128) * 152 bytes (156 for 1-bit) of shared memory per CTA, at most
- * the device's opt-in limit (227 KB on GB300: k <= 24448 at m = 8);
- * beyond it a call returns TQ_ERR_UNSUPPORTED. */
-#define TQ_MAX_ROWS 8
+/* Most activation rows in one call.  A pass of r = min(m, 4) rows also
+ * needs about r * (k/128) * 152 bytes (156 for 1-bit) of shared memory per
+ * CTA besides the weight ring, at most the device's opt-in limit (227 KB on
+ * GB300); beyond it a call returns TQ_ERR_UNSUPPORTED. */
+#define TQ_MAX_ROWS 64
 
 /* Human-readable name of a status code (static string). */
 const char *tq_status_string(tq_status s);

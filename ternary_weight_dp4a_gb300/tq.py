@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libtq.so")
 FMT_TERNARY2 = 0
 FMT_BINARY1 = 1
 BLOCK = 128
-MAX_ROWS = 8
+MAX_ROWS = 64
 
 # every entry point include/tq.h and include/tq_lifecycle.h declare
 EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",

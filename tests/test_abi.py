@@ -75,7 +75,7 @@ def test_gemv_rejects_bad_arguments_before_any_launch(lib):
     assert call(_w(k=200)) == 1                         # k not a multiple of 128
     assert call(_w(n=0)) == 1                           # empty output
     assert call(_w(fmt=7)) == 1                         # unknown format
-    assert call(_w(), m=0) == 1 and call(_w(), m=9) == 1
+    assert call(_w(), m=0) == 1 and call(_w(), m=65) == 1
     assert call(_w(), q=ctypes.c_void_p(0)) == 1
     assert call(_w(codes=0x1010)) == 2                  # codes not 32-byte aligned
     assert call(_w(), q=ctypes.c_void_p(0x3008)) == 2   # q not 16-byte aligned
@@ -91,7 +91,7 @@ def test_ffn_step_rejects_bad_arguments(lib):
         ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), x, m, y, ws, wsb, st)
     assert call(d=_w(n=256, k=384)) == 1                # down shape mismatch
     assert call(u=_w(n=512, k=256, fmt=1)) == 1         # mixed formats
-    assert call(m=9) == 1
+    assert call(m=65) == 1
     assert call(wsb=need - 1) == 4                      # workspace too small
     assert call(ws=ctypes.c_void_p(0x30010)) == 2       # workspace not 256-byte aligned
 
@@ -107,7 +107,7 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.tq_rmsnorm_bf16(None, 1, 128, ctypes.c_float(1e-6), p, st) == 1
     assert lib.tq_ffn_workspace_init(None, 16, st) == 1
     assert lib.tq_ffn_stage_input(p, 1, 256, 512, None, 4096, st) == 1
-    assert lib.tq_ffn_stage_input(p, 9, 256, 512, p, 1 << 20, st) == 1
+    assert lib.tq_ffn_stage_input(p, 65, 256, 512, p, 1 << 20, st) == 1
     big = ctypes.c_void_p(0x100000)
     assert lib.tq_ffn_stage_input(p, 1, 256, 512, big, 16, st) == 4
     assert lib.tq_ffn_stack(None, 1, p, 1, ctypes.c_float(1e-6), p, big, 1 << 20, st) == 1

@@ -148,6 +148,28 @@ def test_gemv_packed_rows_bit_identical_to_single(tq, fmt):
             assert torch.equal(y[r].view(torch.int32), singles[r][0].view(torch.int32)), (m, r)
 
 
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gemv_verify_blocks_up_to_64_rows(tq, orc, fmt):
+    """9..64 rows (verify / prefill blocks) run as passes of at most 4 rows:
+    every row bit-exact against the oracle and bit-identical to its
+    single-row run, including ragged last passes (9, 33 rows)."""
+    import torch
+    n, k = 300, 1152
+    w = Mat(n, k, fmt, seed=23)
+    x = _acts(64, k, 0.01)
+    q_ref, s_ref = orc.rotate_quant(x)
+    q = torch.from_numpy(q_ref).cuda()
+    s = torch.from_numpy(s_ref).cuda()
+    singles = [tq.gemv(w.dev, q[r:r + 1].contiguous(), s[r:r + 1].contiguous()) for r in range(64)]
+    y_ref = orc.gemv(w.orc_packed(orc), w.scales, fmt, n, k, q_ref, s_ref)
+    for m in (9, 16, 33, 64):
+        y = tq.gemv(w.dev, q[:m].contiguous(), s[:m].contiguous())
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref[:m].view(np.uint32)), m
+        for r in range(m):
+            assert torch.equal(y[r].view(torch.int32), singles[r][0].view(torch.int32)), (m, r)
+
+
 # ----------------------------------------------------------------------------
 # FFN step
 # ----------------------------------------------------------------------------
@@ -198,6 +220,14 @@ def _check_ffn(tq, orc, mats, x_bits):
 def test_ffn_step_bit_exact(tq, orc, fmt, hidden, inter, m):
     mats = ffn_mats(hidden, inter, fmt)
     _check_ffn(tq, orc, mats, _acts(m, hidden, 0.01))
+
+
+@pytest.mark.parametrize("m", [9, 33, 64])
+def test_ffn_step_verify_blocks(tq, orc, m):
+    """An FFN step of 9..64 rows (passes of at most 4 rows on one workspace),
+    bit-exact against the oracle row by row."""
+    mats = ffn_mats(256, 1024, 0)
+    _check_ffn(tq, orc, mats, _acts(m, 256, 0.01))
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
