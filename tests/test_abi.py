@@ -120,3 +120,46 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(tq, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         tq.load()
+
+
+def test_headers_are_c11_and_a_c_program_links(lib, tmp_path):
+    """include/*.h compile as pedantic C11 with no warnings, and a C program
+    links against libtq and calls its host-only entry points (no GPU work)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(r'''
+#include "tq.h"
+#include "tq_lifecycle.h"
+#include <stdio.h>
+static void *a(void *c, size_t b, int32_t p) { (void)c; (void)b; (void)p; return 0; }
+static void r(void *c, void *q, size_t b, int32_t p) { (void)c; (void)q; (void)b; (void)p; }
+static size_t f(void *c) { (void)c; return 0; }
+static int32_t bd(void *c, void *q, size_t b) { (void)c; (void)q; (void)b; return 0; }
+int main(void) {
+    tq_lifecycle lc;
+    tq_lifecycle_config cfg = {100, 10, 0, 0};
+    tq_lifecycle_hooks h = {a, r, f, bd, 0};
+    if (tq_lifecycle_init(&lc, &cfg, &h) != TQ_OK) return 1;
+    if (tq_lifecycle_load(&lc) != TQ_OK) return 2;
+    printf("%s %d %zu %zu\n", tq_status_string(TQ_OK), lc.state,
+           tq_ffn_workspace_bytes(1, 5120, 17408), tq_ffn_workspace_error_offset(1, 5120, 17408));
+    return 0;
+}
+''')
+    libdir = os.path.dirname(tq.LIB_PATH)
+    exe = tmp_path / "abi"
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    f"-I{os.path.join(ROOT, 'include')}", str(src), f"-L{libdir}", "-ltq",
+                    "-o", str(exe)], check=True, capture_output=True)
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+    env = dict(os.environ, LD_LIBRARY_PATH=os.pathsep.join(
+        [libdir, cuda_lib, os.environ.get("LD_LIBRARY_PATH", "")]))
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, env=env).stdout.split()
+    assert out[0] == "ok" and int(out[1]) == 2              # skipped: no free memory
+    assert int(out[2]) == lib.tq_ffn_workspace_bytes(1, 5120, 17408)
+    assert int(out[3]) == lib.tq_ffn_workspace_error_offset(1, 5120, 17408)
