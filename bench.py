@@ -42,21 +42,31 @@ SMS = 152
 INT_LANES_PER_CLK = 64       # integer pipe (prmt, lop3, shf, dp4a) per SM and clock, measured
 
 
-def int_ops_per_weight(fmt: int, rows: int) -> float:
-    """Integer-pipe ops per weight in one pass of ``rows`` <= 4 activation rows,
-    counting only the decode and the dot products: 2-bit, 7 ops (3 shifts, 4
-    prmt) per 16 weights plus one dp4a per 4 weights and row; 1-bit, a shift
-    and a mask per 4 weights plus one dp4a per 4 weights and row."""
+ENGINES = {"tcgen05": 2, "dp4a": 1}
+PASS_ROWS = {"tcgen05": 8, "dp4a": 4}
+
+
+def int_ops_per_weight(fmt: int, rows: int, engine: str = "dp4a") -> float:
+    """Integer-pipe ops per weight in one pass of ``rows`` activation rows.
+    dp4a kernel (decode and dot products): 2-bit, 7 ops (3 shifts, 4 prmt) per
+    16 weights plus one dp4a per 4 weights and row; 1-bit, a shift and a mask
+    per 4 weights plus one dp4a per 4 weights and row.  Tensor-core kernel
+    (the decode alone; the tensor core takes the products): 2-bit, the same 7
+    ops per 16 weights; 1-bit, 15 ops (7 shifts, 8 masks) per 32 weights."""
+    if engine == "tcgen05":
+        return 7 / 16 if fmt == 0 else 15 / 32
     return (7 + 4 * rows) / 16 if fmt == 0 else (2 + rows) / 4
 
 
-def alu_bound_us(fmt: int, m: int, weights: int, sm_mhz: float) -> float:
+def alu_bound_us(fmt: int, m: int, weights: int, sm_mhz: float, engine: str = "dp4a") -> float:
     """Time the integer pipe needs for ``weights`` weights at m rows (passes of
-    at most 4 rows, each decoding every weight again) on every SM at
-    ``sm_mhz``: a lower bound on a dp4a step, beside the HBM bound."""
+    at most 4 rows on the dp4a kernel, 8 on the tensor-core kernel, each
+    decoding every weight again) on every SM at ``sm_mhz``: a lower bound
+    beside the HBM bound."""
+    per = PASS_ROWS[engine]
     ops = 0.0
-    for r0 in range(0, m, 4):
-        ops += int_ops_per_weight(fmt, min(4, m - r0))
+    for r0 in range(0, m, per):
+        ops += int_ops_per_weight(fmt, min(per, m - r0), engine)
     return weights * ops / (SMS * INT_LANES_PER_CLK * sm_mhz * 1e6) * 1e6
 
 
@@ -217,20 +227,44 @@ def make_weights(fmt: int, sets: int, hidden: int, inter: int, seed_layer0: int 
     return layers
 
 
-def time_graph(fn_steps, reps: int, warmup_reps: int, world: int, sampler_gpu=None):
-    """Capture fn_steps() (one pass over the weight sets) in a CUDA graph, replay
-    it ``reps`` times in the timed region; returns (ms total, clock summary)."""
+def _capture(fn):
     import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def time_steps(step_fns, steps: int, warmup: int, world: int, sampler_gpu=None):
+    """Time exactly ``steps`` calls of the step functions in rotation
+    (step_fns[0], step_fns[1], ..., wrapping), after exactly ``warmup``
+    untimed ones: one CUDA graph per full pass over the list, replayed, and one
+    of the first (steps mod n) functions for the remainder.  Returns (ms over
+    the timed region between CUDA events on the replaying stream, clock
+    summary sampled meanwhile)."""
+    import torch
+    n = len(step_fns)
+
+    def part(r):
+        def f():
+            for fn in step_fns[:r]:
+                fn()
+        return f
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        fn_steps()                      # eager warm-up outside capture
+        part(n)()                       # eager warm-up of the code paths, outside capture
     torch.cuda.current_stream().wait_stream(s)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        fn_steps()
-    for _ in range(warmup_reps):
-        g.replay()
+    graphs = {n: _capture(part(n))}
+    for r in {steps % n, warmup % n} - {0}:
+        graphs[r] = _capture(part(r))
+
+    def run(count):
+        for _ in range(count // n):
+            graphs[n].replay()
+        if count % n:
+            graphs[count % n].replay()
+    run(warmup)
     torch.cuda.synchronize()
     clocks = None
     ctx = ClockSampler(sampler_gpu) if sampler_gpu is not None else None
@@ -240,8 +274,7 @@ def time_graph(fn_steps, reps: int, warmup_reps: int, world: int, sampler_gpu=No
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    for _ in range(reps):
-        g.replay()
+    run(steps)
     end.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -249,6 +282,11 @@ def time_graph(fn_steps, reps: int, warmup_reps: int, world: int, sampler_gpu=No
         ctx.__exit__(None, None, None)
         clocks = ctx.summary()
     return start.elapsed_time(end), clocks
+
+
+def set_engine(name: str) -> None:
+    from ternary_weight_dp4a_gb300 import tq
+    tq.set_engine(ENGINES[name])
 
 
 # Standalone GEMV shapes (n, k): the tiny config, the FFN's gate/up and down
@@ -263,8 +301,8 @@ GEMV_SHAPES = (("tiny_n512_k256", 512, 256), ("ffn_gate_n17408_k5120", 17408, 51
 
 
 def gemv_sweep(peak: float, fmt: int = 0, ms=(1, 8)):
-    """tq_gemv time per call for each shape and row count, graph-replayed over
-    enough independent weight copies to exceed the 129 MB L2 (at most 64
+    """tq_gemv time per call for each shape, row count and kernel, graph-replayed
+    over enough independent weight copies to exceed the 129 MB L2 (at most 64
     copies: the smallest shapes stay partly L2-resident, said per entry)."""
     import torch
     from ternary_weight_dp4a_gb300 import synth, tq
@@ -284,23 +322,24 @@ def gemv_sweep(peak: float, fmt: int = 0, ms=(1, 8)):
             x = synth.activation(m, k, synth.SEED_ACT_BASE, 0.01, device="cuda")
             q, sc = tq.rotate_quant(x)
             y = torch.empty((m, n), dtype=torch.float32, device="cuda")
-
-            def f():
-                for w in ws:
-                    tq.gemv(w, q, sc, y=y)
-            reps = max(2, 4000 // copies // max(1, wbytes // 2**20 // 8 + 1))
-            t, _ = time_graph(f, reps, 2, 1)
-            us = t * 1e3 / (reps * copies)
-            ent[f"m{m}"] = {"us_per_call": round(us, 3), "weight_gbs": round(wbytes / us / 1e3, 1),
-                            "hbm_frac": round(wbytes / us / 1e3 / peak, 4)}
+            wsp = tq.gemv_workspace(m, n, k)
+            calls = max(copies, min(4000, 400 * copies // max(1, wbytes // 2**20 // 8 + 1)))
+            for eng in ENGINES:
+                set_engine(eng)
+                fns = [lambda w=w: tq.gemv(w, q, sc, y=y, workspace=wsp) for w in ws]
+                t, _ = time_steps(fns, calls, copies, 1)
+                us = t * 1e3 / calls
+                ent[f"m{m}_{eng}"] = {"us_per_call": round(us, 3), "weight_gbs": round(wbytes / us / 1e3, 1),
+                                      "hbm_frac": round(wbytes / us / 1e3 / peak, 4)}
+            set_engine("tcgen05")
         out[name] = ent
         del ws
         torch.cuda.empty_cache()
+    set_engine("tcgen05")
     return out
 
 
 def run_ours(args, rank, world, local):
-    import numpy as np
     import torch
     from ternary_weight_dp4a_gb300 import build as tqbuild
     from ternary_weight_dp4a_gb300 import synth, tq
@@ -316,114 +355,132 @@ def run_ours(args, rank, world, local):
     ys = {m: torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda") for m in xs}
     wss = {m: tq.ffn_workspace(m, HIDDEN, INTER) for m in xs}
 
-    def one_pass(m):
-        def f():
-            for g, u, d in layers:
-                tq.ffn_step(g, u, d, xs[m], y=ys[m], workspace=wss[m])
-        return f
+    def step_fns(m):
+        return [lambda g=g, u=u, d=d: tq.ffn_step(g, u, d, xs[m], y=ys[m], workspace=wss[m])
+                for g, u, d in layers]
 
-    # --- headline: m = 1, K steps (graph of one pass over the N_SETS layers) ---
-    reps = max(1, args.steps // N_SETS)
-    steps = reps * N_SETS
-    warm_reps = max(1, -(-args.warmup // N_SETS))
-    ms, clocks = time_graph(one_pass(1), reps, warm_reps, world, sampler_gpu=local)
+    # --- headline: m = 1, exactly K steps after exactly W warm-up steps, on
+    #     the default kernel (the tensor-core kernel where its plan fits) ---
+    engine = "tcgen05" if tq.get_engine() != ENGINES["dp4a"] else "dp4a"
+    set_engine(engine)
+    ms, clocks = time_steps(step_fns(1), args.steps, args.warmup, world, sampler_gpu=local)
     ms = max_over_ranks(ms, world)
-    ms_step = ms / steps
+    ms_step = ms / args.steps
     value = world * lb / (ms_step * 1e-3) / 1e9
     # the integer-pipe bound uses the SM clock sampled under load (max clock if none)
     sm_mhz = float((clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0)
     layer_w = 3 * HIDDEN * INTER
 
-    # --- batch sweep: packed decode steps m = 1, 2, 4, 8, and verify-sized
-    #     blocks m = 16, 32, 64 (passes of at most 4 rows; same weights) ---
+    # --- the same over a long run (a steady-state figure beside the K-step one) ---
+    steady_steps = max(2000, args.steps)
+    t_st, _ = time_steps(step_fns(1), steady_steps, N_SETS, world)
+    t_st = max_over_ranks(t_st, world)
+    steady = {"steps": steady_steps, "us_per_step": round(t_st * 1e3 / steady_steps, 3),
+              "weight_gbs": round(lb / (t_st * 1e3 / steady_steps) / 1e3, 1),
+              "hbm_frac": round(lb / (t_st * 1e3 / steady_steps) / 1e3 / peak, 4)}
+
+    # --- batch sweep on both kernels: packed decode steps m = 1, 2, 4, 8 and
+    #     verify-sized blocks m = 16, 32, 64 (same weights; one weight stream
+    #     per pass of 8 rows on the tensor-core kernel, 4 on the dp4a kernel).
+    #     This is the measured comparison that decides the kernel. ---
     sweep = {}
     for m in SWEEP_ROWS:
-        # about 2000 steps' worth of weight streams per m (fewer graph replays
-        # for the multi-pass blocks)
-        sweep_reps = max(1, min(reps, 2000 // N_SETS // max(1, m // 8)))
-        t, _ = time_graph(one_pass(m), sweep_reps, 2, world)
-        t = max_over_ranks(t, world)
-        us = t * 1e3 / (sweep_reps * N_SETS)
-        sweep[f"m{m}"] = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
-                          "tokens_per_s": round(m * 1e6 / us, 1),
-                          "hbm_frac": round(lb / us / 1e3 / peak, 4),
-                          "alu_bound_us": round(alu_bound_us(0, m, layer_w, sm_mhz), 3)}
-        sweep[f"m{m}"]["alu_frac"] = round(sweep[f"m{m}"]["alu_bound_us"] / us, 4)
+        for eng in ENGINES:
+            set_engine(eng)
+            passes = -(-m // PASS_ROWS[eng])
+            n_steps = max(N_SETS, min(2000, 2000 // passes))
+            t, _ = time_steps(step_fns(m), n_steps, N_SETS, world)
+            t = max_over_ranks(t, world)
+            us = t * 1e3 / n_steps
+            ent = {"us_per_step": round(us, 3), "weight_gbs": round(lb / us / 1e3, 1),
+                   "tokens_per_s": round(m * 1e6 / us, 1), "hbm_frac": round(lb / us / 1e3 / peak, 4),
+                   "alu_bound_us": round(alu_bound_us(0, m, layer_w, sm_mhz, eng), 3), "steps": n_steps}
+            ent["alu_frac"] = round(ent["alu_bound_us"] / us, 4)
+            sweep[f"m{m}_{eng}"] = ent
+    set_engine(engine)
 
-    # --- roofline: at m = 1 the step is one launch of the persistent step
-    #     kernel (tq_kernel<0,1>: gate/up, SiLU*up, rotation of h, down), so the
-    #     dominant kernel's average launch duration is the headline's timed
-    #     region over its launches (CUDA events on the replaying stream).  The
-    #     figure includes the gap between consecutive launches, so `achieved`
-    #     is a lower bound.  Algorithmic bytes per launch: the layer's codes and
-    #     scales, each read once. ---
-    launches = steps                         # one kernel launch per m = 1 step
+    # --- roofline: at m = 1 a step is one launch of the step kernel (gate/up,
+    #     SiLU*up, rotation of h, down), so the dominant kernel's average launch
+    #     duration is the headline's timed region over its launches (CUDA
+    #     events on the replaying stream).  The figure includes the gap between
+    #     consecutive launches, so `achieved` is a lower bound.  Algorithmic
+    #     bytes per launch: the layer's codes and scales, each read once. ---
+    launches = args.steps                    # one kernel launch per m = 1 step
     k_us = ms * 1e3 / launches
     k_achieved = lb / (k_us * 1e-6) / 1e9
+    kernel_name = ("tq::tc::tc_kernel<0,1> (tensor-core step: gate/up + SiLU*up + h rotation + down)"
+                   if engine == "tcgen05" else
+                   "tq::tq_kernel<0,1,false> (dp4a step: gate/up + SiLU*up + h rotation + down)")
 
     # --- end to end through the public API with pinned host buffers: every step
     #     copies x host->device, runs the step, copies y device->host.  The
-    #     per-step sequence is captured once as a CUDA graph and replayed. ---
+    #     per-step sequence is captured as CUDA graphs and replayed. ---
     x_host = xs[1].cpu().pin_memory()
     y_host = torch.empty((1, HIDDEN), dtype=torch.float32).pin_memory()
     x_dev = torch.empty_like(xs[1])
 
-    def e2e_pass():
-        for g, u, d in layers:
+    def e2e_fns():
+        def one(g, u, d):
             x_dev.copy_(x_host, non_blocking=True)
             tq.ffn_step(g, u, d, x_dev, y=ys[1], workspace=wss[1])
             y_host.copy_(ys[1], non_blocking=True)
+        return [lambda g=g, u=u, d=d: one(g, u, d) for g, u, d in layers]
 
-    e2e_reps = max(1, min(reps, 4000 // N_SETS))
-    t_e2e, _ = time_graph(e2e_pass, e2e_reps, 2, world)
-    e2e_ms = max_over_ranks(t_e2e, world) / (e2e_reps * N_SETS)
+    e2e_steps = max(N_SETS, min(args.steps, 4000))
+    t_e2e, _ = time_steps(e2e_fns(), e2e_steps, N_SETS, world)
+    e2e_ms = max_over_ranks(t_e2e, world) / e2e_steps
     e2e_value = world * lb / (e2e_ms * 1e-3) / 1e9
     # the same with one eager Python call per step (host launch overhead included)
-    for _ in range(2):
-        e2e_pass()
+    fns = e2e_fns()
+    for f in fns:
+        f()
     torch.cuda.synchronize()
-    eager_steps = N_SETS * max(1, min(reps, 1000 // N_SETS))
+    eager_steps = N_SETS * max(1, min(args.steps, 1000) // N_SETS)
     t0 = time.perf_counter()
-    for _ in range(eager_steps // N_SETS):
-        e2e_pass()
+    for i in range(eager_steps):
+        fns[i % N_SETS]()
     torch.cuda.synchronize()
     eager_ms = (time.perf_counter() - t0) * 1e3 / eager_steps
 
-    # --- the 64-layer stacks (2-bit m = 1; 1-bit m = 1, 2, 4, 8) ---
+    # --- the 64-layer stacks (2-bit m = 1; 1-bit m = 1, 2, 4, 8) on both kernels ---
     stacks = {}
     if not args.no_stack:
         del layers
         torch.cuda.empty_cache()
-        for sfmt, ms in ((0, (1,)), (1, (1, 2, 4, 8))):
+        for sfmt, sms in ((0, (1,)), (1, (1, 2, 4, 8))):
             stack_layers = make_weights(sfmt, 64, HIDDEN, INTER)
             sb = 64 * layer_bytes(HIDDEN, INTER, sfmt)
-            for m in ms:
+            for m in sms:
                 xm = synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
                 ym = torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda")
                 wsm = tq.ffn_workspace(m, HIDDEN, INTER)
-                t, _ = time_graph(lambda: tq.ffn_stack(stack_layers, xm, 1e-6, y=ym, workspace=wsm),
-                                  args.stack_reps, 2, world)
-                t = max_over_ranks(t, world)
-                us = t * 1e3 / args.stack_reps
-                alu = alu_bound_us(sfmt, m, 64 * layer_w, sm_mhz)
-                stacks[f"{'ternary2' if sfmt == 0 else 'binary1'}_64L_m{m}"] = {
-                    "us_per_token_step": round(us, 2), "bytes_per_step": sb,
-                    "weight_gbs": round(sb / us / 1e3, 1), "hbm_frac": round(sb / us / 1e3 / peak, 4),
-                    "tokens_per_s": round(m * 1e6 / us, 1),
-                    "alu_bound_us": round(alu, 2), "alu_frac": round(alu / us, 4)}
+                for eng in ENGINES:
+                    set_engine(eng)
+                    fn = [lambda: tq.ffn_stack(stack_layers, xm, 1e-6, y=ym, workspace=wsm)]
+                    t, _ = time_steps(fn, args.stack_reps, 2, world)
+                    t = max_over_ranks(t, world)
+                    us = t * 1e3 / args.stack_reps
+                    alu = alu_bound_us(sfmt, m, 64 * layer_w, sm_mhz, eng)
+                    stacks[f"{'ternary2' if sfmt == 0 else 'binary1'}_64L_m{m}_{eng}"] = {
+                        "us_per_token_step": round(us, 2), "bytes_per_step": sb,
+                        "weight_gbs": round(sb / us / 1e3, 1), "hbm_frac": round(sb / us / 1e3 / peak, 4),
+                        "tokens_per_s": round(m * 1e6 / us, 1),
+                        "alu_bound_us": round(alu, 2), "alu_frac": round(alu / us, 4)}
             del stack_layers
             torch.cuda.empty_cache()
+        set_engine(engine)
 
     # --- standalone GEMV shapes (tq_gemv; weights rotated past L2 where they fit) ---
     gemv = {} if args.no_gemv else gemv_sweep(peak)
+    set_engine(engine)
 
     result = {
         "metric": METRIC,
         "value": round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": steps,
-        "warmup": warm_reps * N_SETS,
+        "steps": args.steps,
+        "warmup": args.warmup,
         "ms_per_step": round(ms_step, 6),
         "us_per_token_m1": round(ms_step * 1e3, 3),
         "higher_is_better": True,
@@ -433,22 +490,24 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded; ternary p0=0.4, fp16 scales U[0.01,0.05], bf16 N(0,1) x, 1% x10 outliers)",
         "config": {"workload": WORKLOAD, "hidden": HIDDEN, "intermediate": INTER, "m": 1,
                    "weight_format": "2-bit ternary, 128-blocks, fp16 scales",
-                   "bytes_per_step": lb, "weight_sets": N_SETS,
+                   "bytes_per_step": lb, "weight_sets": N_SETS, "kernel": engine,
                    "l2": f"{N_SETS} weight sets rotated ({N_SETS * lb / 1e6:.0f} MB > 129 MB L2)",
-                   "timing": "CUDA graph of one pass over the weight sets, replayed; CUDA events",
+                   "timing": "CUDA graphs over the weight sets (a full pass, replayed, and the remainder), "
+                             "exactly --steps timed after exactly --warmup; CUDA events",
                    "parallelism": f"replicas x{world}"},
         "hbm_frac": round(value / world / peak, 4),
+        "steady": steady,
         "sweep": sweep,
         "roofline": {"bound": "hbm",
-                     "kernel": "tq_kernel<0,1,false> (whole FFN step: gate/up + SiLU*up + h rotation + down)",
+                     "kernel": kernel_name,
                      "achieved": round(k_achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(k_achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal": round(k_achieved / NOMINAL_HBM_GBS, 4),
                      "nominal_peak": NOMINAL_HBM_GBS,
-                     "alu_bound_us": round(alu_bound_us(0, 1, layer_w, sm_mhz), 3),
+                     "alu_bound_us": round(alu_bound_us(0, 1, layer_w, sm_mhz, engine), 3),
                      "bytes_per_launch": lb, "avg_launch_us": round(k_us, 3),
                      "launches_timed": launches,
-                     "traffic": recorded_traffic("step_m1")},
+                     "traffic": recorded_traffic(f"step_m1_{engine}")},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "h2d_bytes_per_step": HIDDEN * 2, "d2h_bytes_per_step": HIDDEN * 4,
@@ -462,24 +521,25 @@ def run_ours(args, rank, world, local):
     return result
 
 
-def profile_steps(n: int):
-    """n eager m = 1 steps over the weight sets (no timing, no JSON line)."""
+def profile_steps(n: int, engine: str = "tcgen05", m: int = 1):
+    """n eager m-row steps over the weight sets (no timing, no JSON line)."""
     import torch
     from ternary_weight_dp4a_gb300 import build as tqbuild
     from ternary_weight_dp4a_gb300 import synth, tq
     tqbuild.build()
     tq.load()
+    set_engine(engine)
     layers = make_weights(tq.FMT_TERNARY2, N_SETS, HIDDEN, INTER)
-    x = synth.activation(1, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
-    y = torch.empty((1, HIDDEN), dtype=torch.float32, device="cuda")
-    ws = tq.ffn_workspace(1, HIDDEN, INTER)
+    x = synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
+    y = torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda")
+    ws = tq.ffn_workspace(m, HIDDEN, INTER)
     for i in range(n):
         g, u, d = layers[i % N_SETS]
         tq.ffn_step(g, u, d, x, y=y, workspace=ws)
     torch.cuda.synchronize()
 
 
-def profile_gemv(n: int):
+def profile_gemv(n: int, engine: str = "tcgen05"):
     """n eager m = 1 tq_gemv calls on the 17408 x 5120 gate shape, rotating
     over the weight sets' gate matrices (no timing, no JSON line)."""
     import torch
@@ -487,12 +547,14 @@ def profile_gemv(n: int):
     from ternary_weight_dp4a_gb300 import synth, tq
     tqbuild.build()
     tq.load()
+    set_engine(engine)
     layers = make_weights(tq.FMT_TERNARY2, N_SETS, HIDDEN, INTER)
     x = synth.activation(1, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
     q, s = tq.rotate_quant(x)
     y = torch.empty((1, INTER), dtype=torch.float32, device="cuda")
+    wsp = tq.gemv_workspace(1, INTER, HIDDEN)
     for i in range(n):
-        tq.gemv(layers[i % N_SETS][0], q, s, y=y)
+        tq.gemv(layers[i % N_SETS][0], q, s, y=y, workspace=wsp)
     torch.cuda.synchronize()
 
 
@@ -617,6 +679,9 @@ def main():
                          "(a small, untimed case for a profiler to capture)")
     ap.add_argument("--profile-gemv", type=int, default=0,
                     help="run this many eager m = 1 GEMVs on the 17408 x 5120 gate shape and exit")
+    ap.add_argument("--profile-engine", choices=list(ENGINES), default="tcgen05",
+                    help="kernel for --profile-steps / --profile-gemv")
+    ap.add_argument("--profile-rows", type=int, default=1, help="rows per step for --profile-steps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -643,10 +708,10 @@ def main():
 
     rank, world, local = dist_setup()
     if args.profile_steps > 0:
-        profile_steps(args.profile_steps)
+        profile_steps(args.profile_steps, args.profile_engine, args.profile_rows)
         return
     if args.profile_gemv > 0:
-        profile_gemv(args.profile_gemv)
+        profile_gemv(args.profile_gemv, args.profile_engine)
         return
     result = run_ours(args, rank, world, local)
     if rank == 0:

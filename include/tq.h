@@ -22,9 +22,16 @@
  *     synchronisation, as for any CUDA call.
  *   - Outputs must not overlap inputs or each other.
  *   - Sizes: k and hidden/intermediate are multiples of 128; 1 <= m <= 64.
- *     Rows run in passes of at most 4 through one weight stream each: up to
- *     8 rows is the packed decode step; 9..64 rows (verify or prefill blocks)
- *     run the same passes, each re-reading the weights.
+ *     Rows run in passes through one weight stream each: up to 8 rows per
+ *     pass on the tensor-core kernel (the packed decode step is one pass), up
+ *     to 4 on the dp4a kernel; 9..64 rows (verify or prefill blocks) run
+ *     further passes, each re-reading the weights.
+ *   - Two kernels implement every GEMV and FFN entry point and give
+ *     identical bits: a tensor-core kernel (weights decoded to e4m3 in tensor
+ *     memory, tcgen05.mma against the int8 activation split into two exact
+ *     e4m3 parts) and a dp4a kernel.  tq_set_engine chooses; the default uses
+ *     the tensor-core kernel wherever its shared-memory plan fits the shapes
+ *     and the dp4a kernel elsewhere.
  *   - Floating point is IEEE binary32 with the rounding of each step
  *     documented at the entry point; results do not depend on m, on the
  *     stream or on how many SMs the GPU has.
@@ -57,7 +64,11 @@ typedef enum {
     TQ_ERR_ALIGNMENT = 2,   /* a pointer lacks the alignment its argument needs */
     TQ_ERR_UNSUPPORTED = 3, /* valid but beyond this build's limits              */
     TQ_ERR_WORKSPACE = 4,   /* workspace smaller than tq_ffn_workspace_bytes()   */
-    TQ_ERR_CUDA = 5         /* a CUDA runtime call or launch failed              */
+    TQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed              */
+    TQ_ERR_TIMEOUT = 6      /* a bounded wait inside a kernel ran out (reported
+                               by tq_error_status / tq_read_error_word from a
+                               workspace's error word; the call that launched
+                               the kernel itself returned TQ_OK)                */
 } tq_status;
 
 typedef enum { TQ_FMT_TERNARY2 = 0, TQ_FMT_BINARY1 = 1 } tq_format;
@@ -80,6 +91,33 @@ typedef struct {
 
 /* Human-readable name of a status code (static string). */
 const char *tq_status_string(tq_status s);
+
+/* Kernel selection, process-wide (an atomic setting read at every call):
+ * TQ_ENGINE_AUTO (default) uses the tensor-core kernel where its plan fits and
+ * the dp4a kernel elsewhere; TQ_ENGINE_DP4A always the dp4a kernel;
+ * TQ_ENGINE_TCGEN05 always the tensor-core kernel (a call it cannot serve
+ * returns TQ_ERR_UNSUPPORTED).  Results do not depend on the engine. */
+#define TQ_ENGINE_AUTO 0
+#define TQ_ENGINE_DP4A 1
+#define TQ_ENGINE_TCGEN05 2
+tq_status tq_set_engine(int32_t engine);
+int32_t tq_get_engine(void);
+
+/* Status of an error word read back from a workspace: TQ_OK for 0, else
+ * TQ_ERR_TIMEOUT (the bits say which wait ran out). */
+tq_status tq_error_status(uint32_t error_word);
+
+/* Read the error word at `error_word` (a device address inside a workspace)
+ * after the work enqueued on `stream` so far: copies it to the host and
+ * SYNCHRONISES the stream.  *value (may be NULL) receives the word; returns
+ * tq_error_status(word), or TQ_ERR_CUDA if the copy failed. */
+tq_status tq_read_error_word(const uint32_t *error_word, uint32_t *value, tq_stream_t stream);
+
+/* Zero-fill any libtq workspace (an async memset on `stream`).  A workspace
+ * must be zero-filled once before its first use; every call leaves it
+ * reusable.  After a call that failed in flight (a CUDA error surfaced at
+ * synchronisation, or an error word that is not zero), initialise it again. */
+tq_status tq_workspace_init(void *workspace, size_t workspace_bytes, tq_stream_t stream);
 
 /* cudaError_t of the last failed CUDA call made by this library on the
  * calling thread (0 if none). */
@@ -105,6 +143,9 @@ tq_status tq_pack_weights(const uint8_t *codes, int32_t n, int32_t k, int32_t fm
 tq_status tq_rotate_quant(const uint16_t *x, int32_t m, int32_t k, int8_t *q, float *s,
                           tq_stream_t stream);
 
+/* Bytes of the device workspace tq_gemv needs for an n x k matrix (any m). */
+size_t tq_gemv_workspace_bytes(int32_t m, int32_t n, int32_t k);
+
 /* Ternary/binary GEMV for a packed step of m rows (the "dp4a GEMV", PR #1154
  * Summary).  For row r and output i:
  *   d_b = sum_{j in block b} W[i][j] * q[r][j]          (exact int32)
@@ -117,17 +158,28 @@ tq_status tq_rotate_quant(const uint16_t *x, int32_t m, int32_t k, int8_t *q, fl
  * which is the same for every m, so each row of a packed step is
  * bit-identical to its single-row result.
  * q: int8 [m][k] (16-byte aligned); s: fp32 [m][k/128]; y: fp32 [m][n].
- * blockdots: NULL, or int32 [m][n][k/128] receiving every d_b. */
+ * blockdots: NULL, or int32 [m][n][k/128] receiving every d_b.
+ * workspace: >= tq_gemv_workspace_bytes(m, n, k) bytes, 256-byte aligned,
+ * zero-filled once by tq_workspace_init; its first 4 bytes are the error
+ * word of the bounded waits (bits as for the FFN workspace, plus bit 5 the
+ * tensor-core epilogue, bit 7 its fold queue, bit 8 its operand copies).
+ * The workspace holds the input laid out for the tensor core and every
+ * 128-row tile's segment sums (the tiles' 1024-wide segments are spread
+ * over the SMs and folded by whichever CTA completes the tile).  Calls
+ * sharing a workspace must not run concurrently. */
 tq_status tq_gemv(const tq_weight *w, const int8_t *q, const float *s, int32_t m, float *y,
-                  int32_t *blockdots, tq_stream_t stream);
+                  int32_t *blockdots, void *workspace, size_t workspace_bytes, tq_stream_t stream);
 
 /* The fused gate/up stage of the FFN step: for each row r and output i,
  *   g = gemv(gate, qx, sx)[r][i], u = gemv(up, qx, sx)[r][i]  (as tq_gemv)
  *   h[r][i] = bf16_rn(g / (1 + exp(-g)) * u)                   (as tq_ffn_step)
  * gate, up: [inter][hidden], same format; qx int8 [m][hidden] (16-byte
- * aligned); sx fp32 [m][hidden/128]; h: bf16 bits [m][inter]. */
+ * aligned); sx fp32 [m][hidden/128]; h: bf16 bits [m][inter].
+ * workspace: an FFN workspace for (m, hidden, inter) (see below); its error
+ * word reports a wait that ran out. */
 tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t *qx,
-                        const float *sx, int32_t m, uint16_t *h, tq_stream_t stream);
+                        const float *sx, int32_t m, uint16_t *h, void *workspace,
+                        size_t workspace_bytes, tq_stream_t stream);
 
 /* Bytes of device workspace tq_ffn_step / tq_ffn_stack need for these sizes. */
 size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter);
@@ -142,14 +194,17 @@ size_t tq_ffn_workspace_bytes(int32_t m, int32_t hidden, int32_t inter);
  *   bit 3  a compute warp waited for its unit to be issued
  *   bit 4  the weight stream waited for the input to be staged
  *   bit 6  the down phase waited for a 1024-wide segment of h to be rotated
- * The word stays set until tq_ffn_workspace_init; read it (4 bytes) after
- * synchronising the stream. */
+ *   bit 5  (tensor-core kernel) the epilogue waited for an accumulator, the
+ *          weight scales or the down phase's operand
+ *   bit 7  (tensor-core kernel) the fold warps waited for a job
+ *   bit 8  (tensor-core kernel) the down phase's operand copies at exit
+ * (on the tensor-core kernel bits 0..3 name its weight stream, decoders and
+ * MMA issue in the same order).  The word stays set until the workspace is
+ * initialised again; tq_read_error_word reads it and returns TQ_ERR_TIMEOUT
+ * when it is not zero. */
 size_t tq_ffn_workspace_error_offset(int32_t m, int32_t hidden, int32_t inter);
 
-/* Zero-fill a workspace (an async memset on `stream`).  A workspace must be
- * zero-filled once before its first use; every FFN call leaves it reusable.
- * After a call that failed in flight (a CUDA error surfaced at
- * synchronisation), initialise it again. */
+/* tq_workspace_init under its earlier name. */
 tq_status tq_ffn_workspace_init(void *workspace, size_t workspace_bytes, tq_stream_t stream);
 
 /* One decode FFN step for m packed rows:
@@ -173,14 +228,14 @@ tq_status tq_ffn_workspace_init(void *workspace, size_t workspace_bytes, tq_stre
  * over the calls on the workspace; a launch derives its index from its
  * ticket).  After a call that failed in flight the workspace must be
  * initialised again.  Calls sharing a workspace must not run concurrently.
- * The step is one persistent launch per pass of at most 4 rows (m > 4 runs
- * ceil(m / 4) passes): every CTA first rotates and quantises x into shared
- * memory, then streams its tiles of gate/up; the CTA that completes a
- * 128-block of h rotates and quantises it, and the down phase of each CTA
- * starts on a segment of qh as soon as that segment is ready.  The launch uses
- * programmatic stream serialisation, so it may start while earlier work in
- * the stream drains, reading nothing earlier work writes until that work has
- * completed. */
+ * The step is one persistent launch per pass (at most 8 rows on the
+ * tensor-core kernel, 4 on the dp4a kernel): every CTA first rotates and
+ * quantises x into shared memory, then streams its share of gate/up; the CTA
+ * that completes a 128-block of h rotates and quantises it, and the down
+ * phase of each CTA starts on a segment of h as soon as that segment is
+ * ready.  The launch uses programmatic stream serialisation, so it may start
+ * while earlier work in the stream drains, reading nothing earlier work
+ * writes until that work has completed. */
 tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
                       const uint16_t *x, int32_t m, float *y, void *workspace,
                       size_t workspace_bytes, tq_stream_t stream);
@@ -222,9 +277,13 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
  * intermediate <= TQ_STATIC_MAX_INTER; larger sizes return
  * TQ_ERR_UNSUPPORTED before anything is launched.
  *
+ * The step runs on the dp4a kernel (its part of the workspace is what the
+ * array holds); the bits equal tq_ffn_step's on either engine.
+ *
  * The first call on a device looks up the array's device address for that
- * device (cudaGetSymbolAddress); make that first call before beginning any
- * stream capture.  Each call then zero-fills the part of the array it uses
+ * device (cudaGetSymbolAddress) and keeps it for the life of the process, so
+ * resetting the device (cudaDeviceReset) after that first call is not
+ * supported; make that first call before beginning any stream capture.  Each call then zero-fills the part of the array it uses
  * with an asynchronous memset on `stream` before launching the step.
  * All calls on a device share the one array: calls whose work can overlap on
  * the GPU (different streams without ordering between them) race on it and

@@ -5,7 +5,7 @@
 // (tq_kernel_b.cu), so each compiles half of the instantiations.
 #pragma once
 
-#include <atomic>
+#include <mutex>
 
 #include "tq_kernel.cuh"
 
@@ -16,14 +16,24 @@ constexpr int kMaxDev = 64;
 template <int FMT, int M, bool BO>
 cudaError_t launch_t(const KArgs &a, int grid, size_t bytes, bool coop, cudaStream_t stream) {
     auto kernel = tq_kernel<FMT, M, BO>;
-    static std::atomic<int> configured[kMaxDev] = {};
+    // the attribute is raised once per device, under a lock, to the largest
+    // size any plan can ask for, so concurrent first calls cannot lower it
+    static std::mutex mu;
+    static bool configured[kMaxDev] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= kMaxDev || configured[dev].load() < static_cast<int>(bytes)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-        if (e != cudaSuccess) return e;
-        if (dev < kMaxDev) configured[dev].store(static_cast<int>(bytes));
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= kMaxDev || !configured[dev]) {
+            int optin = 0;
+            if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+                return e;
+            if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 2048)) !=
+                cudaSuccess)
+                return e;
+            if (dev < kMaxDev) configured[dev] = true;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "tq.h"
+#include "tq_workspace.h"
 
 namespace {
 
@@ -16,24 +17,9 @@ constexpr int kStaticMaxRows = TQ_STATIC_MAX_ROWS;
 constexpr int kStaticMaxHidden = TQ_STATIC_MAX_HIDDEN;
 constexpr int kStaticMaxInter = TQ_STATIC_MAX_INTER;
 
-constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-// The FFN workspace at the largest sizes, laid out as tq_ffn_step lays it out
-// (every section 256-byte aligned): qx, sx, h, qh, sh, counters, ybuf, err,
-// sync counters, staged h and its (scale, magic - sum) pairs, h after the
-// first butterfly stages.
-constexpr size_t kStaticBytes =
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden) +
-    align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxHidden / 128) * 4) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter * 2) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
-    align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 4) +
-    align256(static_cast<size_t>(kStaticMaxInter / 128) * 4) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxHidden * 4) + align256(4) +
-    align256(static_cast<size_t>(2 + kStaticMaxInter / 1024) * 4) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter) +
-    align256(static_cast<size_t>(kStaticMaxRows) * (kStaticMaxInter / 128) * 8) +
-    align256(static_cast<size_t>(kStaticMaxRows) * kStaticMaxInter * 4);
+// The dp4a kernel's part of the FFN workspace at the largest sizes (the step
+// this entry point runs; laid out as tq_ffn_step lays it out).
+constexpr size_t kStaticBytes = tq::ffn_layout(kStaticMaxRows, kStaticMaxHidden, kStaticMaxInter).dp4a_total;
 
 // One copy per GPU that loads the library, held until the process exits.
 // Device code could name it directly; host code must use the address from
@@ -48,6 +34,10 @@ void *g_addr[kMaxDevices] = {};
 
 namespace tq {
 void record_cuda_error(int e);
+tq_status ffn_step_dp4a(const tq_weight *gate, const tq_weight *up, const tq_weight *down, const uint16_t *x,
+                        int32_t m, float *y, void *workspace, cudaStream_t str);
+tq_status ffn_check_args(const tq_weight *gate, const tq_weight *up, const tq_weight *down, const uint16_t *x,
+                         int32_t m, const float *y);
 }
 
 namespace {
@@ -63,14 +53,12 @@ size_t tq_ffn_static_workspace_bytes(void) { return kStaticBytes; }
 
 tq_status tq_ffn_step_static(const tq_weight *gate, const tq_weight *up, const tq_weight *down,
                              const uint16_t *x, int32_t m, float *y, tq_stream_t stream) {
-    if (gate == nullptr || up == nullptr || down == nullptr || x == nullptr || y == nullptr)
-        return TQ_ERR_INVALID_ARG;
-    if (m < 1 || m > TQ_MAX_ROWS) return TQ_ERR_INVALID_ARG;
+    tq_status st = tq::ffn_check_args(gate, up, down, x, m, y);
+    if (st != TQ_OK) return st;
     const int hidden = gate->k, inter = gate->n;
     if (m > kStaticMaxRows || hidden > kStaticMaxHidden || inter > kStaticMaxInter)
         return TQ_ERR_UNSUPPORTED;               // beyond the built-in scratch
-    const size_t need = tq_ffn_workspace_bytes(m, hidden, inter);
-    if (need == 0) return TQ_ERR_INVALID_ARG;
+    const size_t need = tq::ffn_layout(m, hidden, inter).dp4a_total;
     if (need > kStaticBytes) return TQ_ERR_UNSUPPORTED;
 
     // set-up, once per device, with that device current: the array's device
@@ -95,7 +83,7 @@ tq_status tq_ffn_step_static(const tq_weight *gate, const tq_weight *up, const t
     // error and barrier words start at zero.
     e = cudaMemsetAsync(ws, 0, need, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e);
-    return tq_ffn_step(gate, up, down, x, m, y, ws, need, stream);
+    return tq::ffn_step_dp4a(gate, up, down, x, m, y, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -18,13 +18,16 @@ LIB_PATH = os.path.join(_PKG, "libtq.so")
 
 FMT_TERNARY2 = 0
 FMT_BINARY1 = 1
+ENGINE_AUTO, ENGINE_DP4A, ENGINE_TCGEN05 = 0, 1, 2
+TQ_ERR_TIMEOUT = 6
 BLOCK = 128
 MAX_ROWS = 64
 
 # every entry point include/tq.h and include/tq_lifecycle.h declare
-EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_pack_weights", "tq_rotate_quant",
-           "tq_gemv", "tq_ffn_gateup", "tq_ffn_workspace_bytes", "tq_ffn_workspace_error_offset",
-           "tq_ffn_workspace_init",
+EXPORTS = ("tq_status_string", "tq_last_cuda_error", "tq_set_engine", "tq_get_engine",
+           "tq_error_status", "tq_read_error_word", "tq_workspace_init", "tq_pack_weights",
+           "tq_rotate_quant", "tq_gemv_workspace_bytes", "tq_gemv", "tq_ffn_gateup",
+           "tq_ffn_workspace_bytes", "tq_ffn_workspace_error_offset", "tq_ffn_workspace_init",
            "tq_ffn_step", "tq_ffn_stage_input", "tq_ffn_stage_gateup", "tq_ffn_stage_down",
            "tq_ffn_stack", "tq_ffn_static_workspace_bytes", "tq_ffn_step_static",
            "tq_rmsnorm_bf16",
@@ -92,8 +95,15 @@ def load():
             L.tq_last_cuda_error.restype = ctypes.c_int
             L.tq_pack_weights.argtypes = [vp, i32, i32, i32, vp, vp]
             L.tq_rotate_quant.argtypes = [vp, i32, i32, vp, vp, vp]
-            L.tq_gemv.argtypes = [W, vp, vp, i32, vp, vp, vp]
-            L.tq_ffn_gateup.argtypes = [W, W, vp, vp, i32, vp, vp]
+            L.tq_set_engine.argtypes = [i32]
+            L.tq_get_engine.argtypes = []
+            L.tq_error_status.argtypes = [ctypes.c_uint32]
+            L.tq_read_error_word.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+            L.tq_workspace_init.argtypes = [vp, sz, vp]
+            L.tq_gemv_workspace_bytes.argtypes = [i32, i32, i32]
+            L.tq_gemv_workspace_bytes.restype = sz
+            L.tq_gemv.argtypes = [W, vp, vp, i32, vp, vp, vp, sz, vp]
+            L.tq_ffn_gateup.argtypes = [W, W, vp, vp, i32, vp, vp, sz, vp]
             L.tq_ffn_workspace_bytes.argtypes = [i32, i32, i32]
             L.tq_ffn_workspace_bytes.restype = sz
             L.tq_ffn_workspace_error_offset.argtypes = [i32, i32, i32]
@@ -124,6 +134,7 @@ def load():
             L.tq_lifecycle_destroy.restype = None
             for name in EXPORTS:
                 if name not in ("tq_status_string", "tq_last_cuda_error", "tq_ffn_workspace_bytes",
+                                "tq_gemv_workspace_bytes",
                                 "tq_ffn_workspace_error_offset", "tq_ffn_static_workspace_bytes", "tq_lifecycle_copy", "tq_lifecycle_alloc",
                                 "tq_lifecycle_free", "tq_lifecycle_release", "tq_lifecycle_destroy"):
                     getattr(L, name).restype = ctypes.c_int
@@ -191,7 +202,36 @@ def rotate_quant(x, q=None, s=None, stream=None):
     return q, s
 
 
-def gemv(w: PackedWeight, q, s, y=None, blockdots: bool = False, stream=None):
+def set_engine(engine: int) -> None:
+    """Process-wide kernel choice: ENGINE_AUTO, ENGINE_DP4A or ENGINE_TCGEN05."""
+    _check("tq_set_engine", load().tq_set_engine(engine))
+
+
+def get_engine() -> int:
+    return int(load().tq_get_engine())
+
+
+def read_error_word(word_tensor, stream=None) -> int:
+    """Read a workspace's error word (a 4-byte slice of the workspace tensor)
+    through tq_read_error_word: synchronises the stream; raises TQError with
+    status TQ_ERR_TIMEOUT when the word is not zero, else returns 0."""
+    v = ctypes.c_uint32(0)
+    st = load().tq_read_error_word(_ptr(word_tensor), ctypes.byref(v), _stream(stream))
+    _check("tq_read_error_word", st)
+    return int(v.value)
+
+
+def gemv_workspace_bytes(m: int, n: int, k: int) -> int:
+    return int(load().tq_gemv_workspace_bytes(m, n, k))
+
+
+def gemv_workspace(m: int, n: int, k: int, device="cuda"):
+    """A zero-filled GEMV workspace (its first 4 bytes are the error word)."""
+    import torch
+    return torch.zeros(gemv_workspace_bytes(m, n, k), dtype=torch.uint8, device=device)
+
+
+def gemv(w: PackedWeight, q, s, y=None, blockdots: bool = False, workspace=None, stream=None):
     """y[m][n] (float32); with ``blockdots`` also the int32 [m][n][k/128] dots."""
     import torch
     m = q.shape[0]
@@ -199,21 +239,26 @@ def gemv(w: PackedWeight, q, s, y=None, blockdots: bool = False, stream=None):
         y = torch.empty((m, w.n), dtype=torch.float32, device=q.device)
     d = torch.empty((m, w.n, w.k // BLOCK), dtype=torch.int32, device=q.device) \
         if blockdots else None
+    if workspace is None:
+        workspace = gemv_workspace(m, w.n, w.k, q.device)
     ws = w.c_struct()
     _check("tq_gemv", load().tq_gemv(ctypes.byref(ws), _ptr(q), _ptr(s), m, _ptr(y), _ptr(d),
-                                     _stream(stream)))
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
     return (y, d) if blockdots else y
 
 
-def ffn_gateup(gate: PackedWeight, up: PackedWeight, qx, sx, h=None, stream=None):
+def ffn_gateup(gate: PackedWeight, up: PackedWeight, qx, sx, h=None, workspace=None, stream=None):
     """Fused gate/up GEMVs + SiLU(g)*u: qx int8 [m][hidden] -> h bf16 [m][inter]."""
     import torch
     m = qx.shape[0]
     if h is None:
         h = torch.empty((m, gate.n), dtype=torch.bfloat16, device=qx.device)
+    if workspace is None:
+        workspace = ffn_workspace(m, gate.k, gate.n, qx.device)
     g, u = gate.c_struct(), up.c_struct()
     _check("tq_ffn_gateup", load().tq_ffn_gateup(ctypes.byref(g), ctypes.byref(u), _ptr(qx),
-                                                 _ptr(sx), m, _ptr(h), _stream(stream)))
+                                                 _ptr(sx), m, _ptr(h), _ptr(workspace),
+                                                 workspace.numel(), _stream(stream)))
     return h
 
 

@@ -17,14 +17,24 @@ def round_up(x, a):
 
 def ws_offsets(m, hidden, inter):
     """Offsets of the FFN-step intermediates inside the workspace (qx, sx, h,
-    qh, sh, counters, ybuf), as tq_ffn_step lays them out; used only to read
-    intermediates back for stage-wise diagnosis."""
+    qh, sh, counters, ybuf, ..., and the tensor-core kernel's sections), as
+    tq_ffn_step lays them out; used only to read intermediates and the
+    synchronisation state back for diagnosis."""
+    def cdiv(a, b):
+        return (a + b - 1) // b
+    seg_blocks = cdiv(inter // B, 8) * 8
+    passes = cdiv(m, 8)
     off, o = 0, {}
     for name, nbytes in (("qx", m * hidden), ("sx", m * (hidden // B) * 4),
                          ("h", m * inter * 2), ("qh", m * inter), ("sh", m * (inter // B) * 4),
                          ("counters", (inter // B) * 4), ("ybuf", m * hidden * 4), ("err", 4),
                          ("sync", (2 + (inter + 1023) // 1024) * 4), ("hst", m * inter), ("hsn", m * (inter // B) * 8),
-                         ("hp", m * inter * 4)):
+                         ("hp", m * inter * 4),
+                         ("tc_hst", passes * seg_blocks * 2048), ("tc_hsn", passes * seg_blocks * 64),
+                         ("part_a", 2 * cdiv(inter, B) * cdiv(hidden // B, 8) * 8 * B * 4),
+                         ("part_b", cdiv(hidden, B) * cdiv(inter // B, 8) * 8 * B * 4),
+                         ("cnt_a", cdiv(inter, B) * 4), ("cnt_b", cdiv(hidden, B) * 4),
+                         ("ybuf2", m * hidden * 4)):
         o[name] = off
         off = round_up(off + nbytes, 256)
     o["total"] = off

@@ -42,16 +42,43 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     assert lib.tq_status_string(0) == b"ok"
     assert lib.tq_status_string(4) == b"workspace too small"
+    assert lib.tq_status_string(6).startswith(b"a bounded wait")
     assert lib.tq_status_string(99) == b"unknown status"
 
 
+def test_error_word_maps_to_timeout_status(lib):
+    assert lib.tq_error_status(0) == 0
+    for bit in range(9):
+        assert lib.tq_error_status(1 << bit) == tq.TQ_ERR_TIMEOUT
+    assert lib.tq_read_error_word(None, None, ctypes.c_void_p(0)) == 1
+
+
+def test_engine_setting_round_trips_and_rejects_unknown(lib):
+    before = lib.tq_get_engine()
+    try:
+        for e in (tq.ENGINE_DP4A, tq.ENGINE_TCGEN05, tq.ENGINE_AUTO):
+            assert lib.tq_set_engine(e) == 0 and lib.tq_get_engine() == e
+        assert lib.tq_set_engine(7) == 1 and lib.tq_get_engine() == tq.ENGINE_AUTO
+    finally:
+        lib.tq_set_engine(before)
+
+
 def test_workspace_bytes(lib):
-    # qx 5120 | sx 160->256 | h 34816 | qh 17408 | sh 544->768 | counters 544->768 |
-    # ybuf 20480 | err 4->256 | sync 76->256 | hst 17408 | hsn 1088->1280 | hp 69632,
-    # each 256-aligned
-    assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == \
-        5120 + 256 + 34816 + 17408 + 768 + 768 + 20480 + 256 + 256 + 17408 + 1280 + 69632
+    # dp4a part: qx 5120 | sx 160->256 | h 34816 | qh 17408 | sh 544->768 |
+    # counters 544->768 | ybuf 20480 | err 4->256 | sync 76->256 | hst 17408 |
+    # hsn 1088->1280 | hp 69632, each 256-aligned
+    dp4a = 5120 + 256 + 34816 + 17408 + 768 + 768 + 20480 + 256 + 256 + 17408 + 1280 + 69632
+    # tensor-core part: operand copy of h, 136 blocks x 2 KB | its pairs 136 x 8 x 8 |
+    # segment sums of gate and up, 2 x 136 tiles x 5 segments x 8 rows x 128 x 4 |
+    # of down, 40 tiles x 17 segments x 4096 | tile counts 136 x 4 -> 768, 40 x 4 -> 256 |
+    # second stack buffer 20480
+    tc = 136 * 2048 + 136 * 64 + 2 * 136 * 5 * 4096 + 40 * 17 * 4096 + 768 + 256 + 20480
+    assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == dp4a + tc
     assert lib.tq_ffn_workspace_bytes(0, 5120, 17408) == 0
+    # GEMV: err 256 | tile counts 136 x 4 -> 768 | operand 40 blocks x 2 KB |
+    # pairs 40 x 64 | segment sums 136 tiles x 5 segments x 4096
+    assert lib.tq_gemv_workspace_bytes(1, 17408, 5120) == 256 + 768 + 40 * 2048 + 40 * 64 + 136 * 5 * 4096
+    assert lib.tq_gemv_workspace_bytes(0, 17408, 5120) == 0
 
 
 def test_workspace_error_offset(lib):
@@ -70,7 +97,9 @@ def _w(codes=0x1000, scales=0x2000, n=512, k=256, fmt=0):
 def test_gemv_rejects_bad_arguments_before_any_launch(lib):
     good_q, good_s, good_y = ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000), ctypes.c_void_p(0x5000)
     st = ctypes.c_void_p(0)
-    call = lambda w, q=good_q, s=good_s, m=1, y=good_y: lib.tq_gemv(ctypes.byref(w), q, s, m, y, None, st)
+    ws, wsb = ctypes.c_void_p(0x100000), lib.tq_gemv_workspace_bytes(1, 512, 256)
+    call = lambda w, q=good_q, s=good_s, m=1, y=good_y, ws=ws, wsb=wsb: lib.tq_gemv(
+        ctypes.byref(w), q, s, m, y, None, ws, wsb, st)
     assert call(_w(codes=0)) == 1                       # null codes
     assert call(_w(k=200)) == 1                         # k not a multiple of 128
     assert call(_w(n=0)) == 1                           # empty output
@@ -79,7 +108,14 @@ def test_gemv_rejects_bad_arguments_before_any_launch(lib):
     assert call(_w(), q=ctypes.c_void_p(0)) == 1
     assert call(_w(codes=0x1010)) == 2                  # codes not 32-byte aligned
     assert call(_w(), q=ctypes.c_void_p(0x3008)) == 2   # q not 16-byte aligned
-    assert lib.tq_gemv(None, good_q, good_s, 1, good_y, None, st) == 1
+    assert call(_w(), ws=ctypes.c_void_p(0)) == 1       # no workspace
+    assert call(_w(), ws=ctypes.c_void_p(0x100010)) == 2  # workspace not 256-byte aligned
+    assert call(_w(), wsb=wsb - 1) == 4                 # workspace too small
+    assert lib.tq_gemv(None, good_q, good_s, 1, good_y, None, ws, wsb, st) == 1
+    g, u = _w(n=512, k=256), _w(n=512, k=256)
+    fw = lib.tq_ffn_workspace_bytes(1, 256, 512)
+    assert lib.tq_ffn_gateup(ctypes.byref(g), ctypes.byref(u), good_q, good_s, 1, good_y, ws, fw - 1, st) == 4
+    assert lib.tq_ffn_gateup(ctypes.byref(g), ctypes.byref(u), good_q, good_s, 1, good_y, None, fw, st) == 1
 
 
 def test_ffn_step_rejects_bad_arguments(lib):
@@ -145,8 +181,11 @@ int main(void) {
     tq_lifecycle_hooks h = {a, r, f, bd, 0};
     if (tq_lifecycle_init(&lc, &cfg, &h) != TQ_OK) return 1;
     if (tq_lifecycle_load(&lc) != TQ_OK) return 2;
-    printf("%s %d %zu %zu\n", tq_status_string(TQ_OK), lc.state,
-           tq_ffn_workspace_bytes(1, 5120, 17408), tq_ffn_workspace_error_offset(1, 5120, 17408));
+    if (tq_set_engine(TQ_ENGINE_DP4A) != TQ_OK || tq_get_engine() != TQ_ENGINE_DP4A) return 3;
+    if (tq_error_status(64u) != TQ_ERR_TIMEOUT) return 4;
+    printf("%s %d %zu %zu %zu\n", tq_status_string(TQ_OK), lc.state,
+           tq_ffn_workspace_bytes(1, 5120, 17408), tq_ffn_workspace_error_offset(1, 5120, 17408),
+           tq_gemv_workspace_bytes(1, 17408, 5120));
     return 0;
 }
 ''')
@@ -163,3 +202,4 @@ int main(void) {
     assert out[0] == "ok" and int(out[1]) == 2              # skipped: no free memory
     assert int(out[2]) == lib.tq_ffn_workspace_bytes(1, 5120, 17408)
     assert int(out[3]) == lib.tq_ffn_workspace_error_offset(1, 5120, 17408)
+    assert int(out[4]) == lib.tq_gemv_workspace_bytes(1, 17408, 5120)

@@ -490,3 +490,96 @@ def test_mutants_are_rejected(orc):
     old = np.float32(np.float32(np.float32(parts[0] + parts[1]) + np.float32(parts[2] + parts[3]))
                      + np.float32(np.float32(parts[4] + parts[5]) + np.float32(parts[6] + parts[7])))
     assert old == np.float32(2.0) and old != want
+
+# ----------------------------------------------------------------------------
+# the layer stack: layer l + 1 reads the RMS-normalised output of layer l
+# ----------------------------------------------------------------------------
+
+def _stack_identity_closed_form(c, n_layers, eps, sg, su, sd):
+    """y of a stack of identity-weight layers (hidden = inter = 128, +1 on the
+    diagonal; every gate / up / down scale sg / su / sd) fed x = c * e_0, derived
+    by hand from the definitions, step by step in binary32:
+
+    * rotation of c * e_0: every butterfly adds or subtracts an exact zero, so
+      all 128 values are c, times k = (float)(1/sqrt(128)); absmax = |c k|,
+      s = absmax / 127, and every code is rint((c k) / s) = +-127.
+    * gate / up: one block, one segment, so g = 0 + 127 (sg s) and
+      u = 127 (su s) in every output (with the sign of c).
+    * h = bf16(silu(g) u) is the same in all 128 outputs; its rotation is
+      128 h k at index 0 and exact zeros elsewhere, so s_h = |128 h k| / 127,
+      code 0 is +-127 and the rest 0: y = (127 (sd s_h) sign, 0, ..., 0).
+    * RMS-normalise of that y: the sum of squares is y_0^2 exactly, so the next
+      input is bf16(y_0 / sqrt(y_0^2 / 128 + eps)) * e_0.
+    The last layer's y is not normalised."""
+    f = np.float32
+    k = np.uint32(0x3DB504F3).view(np.float32)
+    x0 = f(c)
+    y0 = None
+    for layer in range(n_layers):
+        v = f(x0 * k)
+        s = f(abs(v) / f(127))
+        q = f(127) if v > 0 else f(-127)
+        g = f(q * f(f(sg) * s))
+        u = f(q * f(f(su) * s))
+        gd, ud = float(g), float(u)
+        h64 = gd / (1.0 + math.exp(-gd)) * ud
+        hb = _bf16_bits(np.array([h64], np.float32))[0]
+        hv = _bf16_value(np.array([hb]))[0]
+        # the fp32 chain of the oracle rounds to the same bf16 value unless
+        # h64 sits within an fp32 ulp or two of a bf16 rounding midpoint
+        lo, hi = sorted((float(_bf16_value(np.array([hb - 1]))[0]), float(_bf16_value(np.array([hb + 1]))[0])))
+        assert abs(h64 - (hv + lo) / 2) > 1e-5 * abs(h64) and abs(h64 - (hv + hi) / 2) > 1e-5 * abs(h64)
+        vh = f(f(f(128) * hv) * k)
+        sh = f(abs(vh) / f(127))
+        qh = f(127) if vh > 0 else f(-127)
+        y0 = f(qh * f(f(sd) * sh))
+        if layer + 1 < n_layers:
+            ms = f(f(y0 * y0) / f(128))
+            inv = f(f(1) / np.sqrt(f(ms + f(eps)), dtype=np.float32))
+            x0 = _bf16_value(_bf16_bits(np.array([f(y0 * inv)], np.float32)))[0]
+    y = np.zeros(128, np.float32)
+    y[0] = y0
+    return y
+
+
+def _identity_stack_layers(orc, n_layers, sg, su, sd):
+    n = B
+    P = orc.pack(np.eye(n, dtype=np.uint8), 0)
+    sc = [np.full((n, 1), v, np.float16) for v in (sg, su, sd)]
+    return [(P, sc[0], P, sc[1], P, sc[2])] * n_layers
+
+
+@pytest.mark.parametrize("c,eps", [(3.0, 1e-6), (-0.75, 0.01)])
+def test_ffn_stack_identity_closed_form(orc, c, eps):
+    sg, su, sd = 1.0, 0.5, 2.0
+    x = _bf16_bits(np.array([[c] + [0.0] * (B - 1)], np.float32))
+    for n_layers in (1, 2, 3):
+        layers = _identity_stack_layers(orc, n_layers, sg, su, sd)
+        y = orc.ffn_stack(layers, 0, B, B, x, eps)
+        want = _stack_identity_closed_form(c, n_layers, eps, sg, su, sd)
+        assert np.array_equal(y[0].view(np.uint32), want.view(np.uint32)), (n_layers, y[0][:2], want[:2])
+
+
+def test_ffn_stack_mutants_are_rejected(orc):
+    """Plausible mistakes in the stack's composition fail the closed-form pin:
+    normalising after the last layer, feeding layer 2 the raw input instead of
+    the normalised output of layer 1, and dropping (or misplacing) eps."""
+    sg, su, sd, c, eps = 1.0, 0.5, 2.0, 3.0, 0.01
+    x = _bf16_bits(np.array([[c] + [0.0] * (B - 1)], np.float32))
+    layers = _identity_stack_layers(orc, 2, sg, su, sd)
+    want = _stack_identity_closed_form(c, 2, eps, sg, su, sd)
+    good = orc.ffn_stack(layers, 0, B, B, x, eps)[0]
+    assert np.array_equal(good.view(np.uint32), want.view(np.uint32))
+    # the last layer normalised as well
+    normed_last = _bf16_value(orc.rmsnorm_bf16(good[None, :], eps))[0]
+    assert not np.array_equal(normed_last, want)
+    # layer 2 fed x instead of rmsnorm(y_1)
+    y1 = orc.ffn_step(*layers[0], 0, B, B, x)["y"]
+    raw = orc.ffn_step(*layers[1], 0, B, B, x)["y"][0]
+    assert not np.array_equal(raw, want)
+    # layer 2 fed y_1 rounded to bf16 without the normalisation
+    unnormed = orc.ffn_step(*layers[1], 0, B, B, _bf16_bits(y1))["y"][0]
+    assert not np.array_equal(unnormed, want)
+    # eps dropped (0 instead of the argument)
+    no_eps = orc.ffn_stack(layers, 0, B, B, x, 0.0)[0]
+    assert not np.array_equal(no_eps, want)

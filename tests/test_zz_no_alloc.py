@@ -28,9 +28,10 @@ def tq():
     return tqmod
 
 
-# (1024, 3072, 1) runs the fused single-kernel step, (1024, 2816, 3) the
-# three-kernel step
-@pytest.mark.parametrize("hidden,inter,m", [(1024, 3072, 1), (1024, 2816, 3)])
+# one row; 3 rows (one pass); 5 and 8 rows (two passes over the one array: the
+# launch ticket, the segment counters and the per-block counts carry from the
+# first pass to the second after a single zero-fill)
+@pytest.mark.parametrize("hidden,inter,m", [(1024, 3072, 1), (1024, 2816, 3), (1024, 2816, 5), (2048, 4096, 8)])
 def test_static_scratch_step_matches_workspace_step(tq, hidden, inter, m):
     import torch
     g, u, d = (w.dev for w in ffn_mats(hidden, inter, 0))
@@ -41,6 +42,39 @@ def test_static_scratch_step_matches_workspace_step(tq, hidden, inter, m):
         y_ref = tq.ffn_step(g, u, d, x)
         torch.cuda.synchronize()
         assert torch.equal(y_static.view(torch.int32), y_ref.view(torch.int32)), call
+
+
+def test_static_scratch_call_allocates_nothing(tq):
+    """After a first call (which looks the array up once), a raw C-ABI call
+    changes neither PyTorch's allocation counters nor the device's free
+    memory: the entry point allocates nothing."""
+    import torch
+    hidden, inter, m = 1024, 2816, 2
+    g, u, d = (w.dev for w in ffn_mats(hidden, inter, 0))
+    x = bf16_tensor(synth.activation(m, hidden, seed=synth.SEED_ACT_BASE, outlier_frac=0.01))
+    y = torch.empty((m, hidden), dtype=torch.float32, device="cuda")
+    lib = tq.load()
+    gs, us, ds = g.c_struct(), u.c_struct(), d.c_struct()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call():
+        return lib.tq_ffn_step_static(ctypes.byref(gs), ctypes.byref(us), ctypes.byref(ds),
+                                      ctypes.c_void_p(x.data_ptr()), m, ctypes.c_void_p(y.data_ptr()), stream)
+    assert call() == 0
+    torch.cuda.synchronize()
+    stats0 = torch.cuda.memory_stats()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        assert call() == 0
+    torch.cuda.synchronize()
+    stats1 = torch.cuda.memory_stats()
+    free1 = torch.cuda.mem_get_info()[0]
+    for key in ("allocation.all.allocated", "segment.all.allocated", "reserved_bytes.all.current"):
+        assert stats1.get(key, 0) == stats0.get(key, 0), key
+    assert free1 == free0
+    ref = tq.ffn_step(g, u, d, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), ref.view(torch.int32))
 
 
 def test_static_scratch_refuses_sizes_beyond_its_limit(tq):
