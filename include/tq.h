@@ -27,11 +27,11 @@
  *     to 4 on the dp4a kernel; 9..64 rows (verify or prefill blocks) run
  *     further passes, each re-reading the weights.
  *   - Two kernels implement every GEMV and FFN entry point and give
- *     identical bits: a tensor-core kernel (weights decoded to e4m3 in tensor
- *     memory, tcgen05.mma against the int8 activation split into two exact
- *     e4m3 parts) and a dp4a kernel.  tq_set_engine chooses; the default uses
- *     the tensor-core kernel wherever its shared-memory plan fits the shapes
- *     and the dp4a kernel elsewhere.
+ *     identical bits: a dp4a kernel and a tensor-core kernel (weights decoded
+ *     to e4m3 in tensor memory, tcgen05.mma against the int8 activation split
+ *     into two exact e4m3 parts).  tq_set_engine chooses; the default uses the
+ *     dp4a kernel, measured the faster on GB300 at every row count, wherever
+ *     its shared-memory plan fits, and the tensor-core kernel elsewhere.
  *   - Floating point is IEEE binary32 with the rounding of each step
  *     documented at the entry point; results do not depend on m, on the
  *     stream or on how many SMs the GPU has.
@@ -93,8 +93,8 @@ typedef struct {
 const char *tq_status_string(tq_status s);
 
 /* Kernel selection, process-wide (an atomic setting read at every call):
- * TQ_ENGINE_AUTO (default) uses the tensor-core kernel where its plan fits and
- * the dp4a kernel elsewhere; TQ_ENGINE_DP4A always the dp4a kernel;
+ * TQ_ENGINE_AUTO (default) uses the dp4a kernel where its plan fits and the
+ * tensor-core kernel elsewhere; TQ_ENGINE_DP4A always the dp4a kernel;
  * TQ_ENGINE_TCGEN05 always the tensor-core kernel (a call it cannot serve
  * returns TQ_ERR_UNSUPPORTED).  Results do not depend on the engine. */
 #define TQ_ENGINE_AUTO 0

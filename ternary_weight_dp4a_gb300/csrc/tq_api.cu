@@ -3,9 +3,10 @@
 // pointer owned by the caller; nothing here allocates.
 //
 // Two kernels compute every GEMV and FFN entry point with identical results:
-// the tensor-core kernel (tq_tc_kernel.cuh, passes of up to 8 rows) and the
-// dp4a kernel (tq_kernel.cuh, passes of up to 4 rows).  The engine setting
-// picks one; the default takes the tensor-core kernel wherever its plan fits.
+// the dp4a kernel (tq_kernel.cuh) and the tensor-core kernel
+// (tq_tc_kernel.cuh, passes of up to 8 rows).  The engine setting picks one;
+// the default takes the dp4a kernel (the faster, measured) wherever its
+// shared-memory plan fits.
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
@@ -137,16 +138,27 @@ constexpr int kTcPass = 8;
 int pass_rows(int m, int r0, int per) { return m - r0 < per ? m - r0 : per; }
 
 // ---- engine choice -----------------------------------------------------------
-// The tensor-core kernel's plan for a pass of min(m, 8) rows decides for the
-// whole call (a smaller last pass needs less).  Returns TQ_OK with *tc set,
-// or an error (TQ_ERR_UNSUPPORTED when the tensor-core engine is forced and
-// does not fit, TQ_ERR_CUDA when the device query fails).
-tq_status choose_engine(tq::TcCall c, int m, bool *tc) {
+// TQ_ENGINE_AUTO takes the dp4a kernel: measured on GB300 it is the faster of
+// the two at every row count (a tcgen05.mma of M = 128, K = 32 costs ~145
+// cycles whatever N is, so the tensor-core kernel cannot stream the weights
+// faster than ~30 us per 71 MB FFN layer, and its pipeline's latencies add
+// to that), and the tensor-core kernel only where the dp4a kernel's plan
+// does not fit.  The tensor-core kernel's plan for a pass of min(m, 8) rows
+// decides for the whole call (a smaller last pass needs less).  Returns TQ_OK
+// with *tc set, or an error (TQ_ERR_UNSUPPORTED when the tensor-core engine
+// is forced and does not fit, TQ_ERR_CUDA when a device query fails).
+tq_status choose_engine(tq::TcCall c, int m, bool *tc, const tq::Call *dp4a_fallback = nullptr) {
     const int engine = g_engine.load();
     *tc = false;
     if (engine == TQ_ENGINE_DP4A) return TQ_OK;
-    c.m = m < kTcPass ? m : kTcPass;
     cudaError_t e = cudaSuccess;
+    if (engine == TQ_ENGINE_AUTO) {
+        if (dp4a_fallback == nullptr) return TQ_OK;
+        const bool dp4a_fits = tq::call_fits(*dp4a_fallback, &e);
+        if (e != cudaSuccess) return cuda_status(e);
+        if (dp4a_fits) return TQ_OK;
+    }
+    c.m = m < kTcPass ? m : kTcPass;
     const bool ok = tq::tc_applicable(c, &e);
     if (e != cudaSuccess) return cuda_status(e);
     if (!ok && engine == TQ_ENGINE_TCGEN05) return TQ_ERR_UNSUPPORTED;
@@ -367,8 +379,9 @@ tq_status tq_gemv(const tq_weight *w, const int8_t *q, const float *s, int32_t m
     cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     tq::TcCall tc = tc_call(nullptr, nullptr, w, w->fmt);
+    const tq::Call dpc = dp4a_call(nullptr, nullptr, w, w->fmt);
     bool use_tc = false;
-    if ((st = choose_engine(tc, m, &use_tc)) != TQ_OK) return st;
+    if ((st = choose_engine(tc, m, &use_tc, &dpc)) != TQ_OK) return st;
     if (use_tc) {
         uint8_t *bst = wsb + L.operand;
         float2 *bsn = reinterpret_cast<float2 *>(wsb + L.pairs);
@@ -434,8 +447,9 @@ tq_status tq_ffn_gateup(const tq_weight *gate, const tq_weight *up, const int8_t
     cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     tq::TcCall tc = tc_call(gate, up, nullptr, gate->fmt);
+    const tq::Call dpc = dp4a_call(gate, up, nullptr, gate->fmt);
     bool use_tc = false;
-    if ((st = choose_engine(tc, m, &use_tc)) != TQ_OK) return st;
+    if ((st = choose_engine(tc, m, &use_tc, &dpc)) != TQ_OK) return st;
     if (use_tc) {
         tc.in_mode = tq::kInPlain;
         tc.part_a = P.part_a;
@@ -493,8 +507,9 @@ tq_status tq_ffn_stage_gateup(const tq_weight *gate, const tq_weight *up, int32_
     cudaError_t e = cudaSuccess;
     tq::TcCall tc = tc_call(gate, up, nullptr, gate->fmt);
     tc.rotate_h = 1;
+    const tq::Call dpc = dp4a_call(gate, up, nullptr, gate->fmt);
     bool use_tc = false;
-    if ((st = choose_engine(tc, m, &use_tc)) != TQ_OK) return st;
+    if ((st = choose_engine(tc, m, &use_tc, &dpc)) != TQ_OK) return st;
     if (use_tc) {
         tc.in_mode = tq::kInPlain;
         for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += kTcPass) {
@@ -537,8 +552,9 @@ tq_status tq_ffn_stage_down(const tq_weight *down, int32_t m, float *y, void *wo
     cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     tq::TcCall tc = tc_call(nullptr, nullptr, down, down->fmt);
+    const tq::Call dpc = dp4a_call(nullptr, nullptr, down, down->fmt);
     bool use_tc = false;
-    if ((st = choose_engine(tc, m, &use_tc)) != TQ_OK) return st;
+    if ((st = choose_engine(tc, m, &use_tc, &dpc)) != TQ_OK) return st;
     if (use_tc) {
         for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += kTcPass) {
             tc.m = pass_rows(m, r0, kTcPass);
@@ -574,8 +590,9 @@ tq_status tq_ffn_step(const tq_weight *gate, const tq_weight *up, const tq_weigh
     cudaStream_t str = reinterpret_cast<cudaStream_t>(stream);
     tq::TcCall tc = tc_call(gate, up, down, gate->fmt);
     tc.rotate_h = 1;
+    const tq::Call dpc = dp4a_call(gate, up, down, gate->fmt);
     bool use_tc = false;
-    if ((st = choose_engine(tc, m, &use_tc)) != TQ_OK) return st;
+    if ((st = choose_engine(tc, m, &use_tc, &dpc)) != TQ_OK) return st;
     if (!use_tc) return tq::ffn_step_dp4a(gate, up, down, x, m, y, workspace, str);
     const FfnPtrs P = ffn_ptrs(workspace, L);
     cudaError_t e = cudaSuccess;
@@ -611,8 +628,9 @@ tq_status tq_ffn_stack(const tq_weight *layers, int32_t num_layers, const uint16
     cudaError_t e = cudaSuccess;
     tq::TcCall tc = tc_call(&layers[0], &layers[1], &layers[2], layers[0].fmt);
     tc.rotate_h = 1;
+    const tq::Call dpc = dp4a_call(&layers[0], &layers[1], &layers[2], layers[0].fmt);
     bool use_tc = false;
-    if ((st = choose_engine(tc, m, &use_tc)) != TQ_OK) return st;
+    if ((st = choose_engine(tc, m, &use_tc, &dpc)) != TQ_OK) return st;
     // rows are independent through the whole stack: each pass of rows runs
     // every layer; a layer after the first starts from the RMS-normalised
     // output of the one before

@@ -780,39 +780,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 #pragma unroll
                 for (int r = 0; r < M; ++r) acc[r] = 0.0f;
                 int32_t *dots = U.phase == 1 ? a.dots : nullptr;
-                // the unit's blocks in groups of up to kEpiGroup (group G in slot
-                // G mod kGroupSlots): one wait, every load in flight together,
-                // one wait for them, one release
-                for (int b0 = 0; b0 < U.bcount && ok; b0 += kEpiGroup, ++Ge) {
-                    const int nb_g = min(kEpiGroup, U.bcount - b0);
-                    const int gs = Ge % kGroupSlots, gr = Ge / kGroupSlots;
-                    if (!(ok = __all_sync(0xffffffffu, tc_wait(smem_u32(&d_full[gs]), gr & 1, abort_flag, 32u, bad))))
-                        break;
-                    tc_fence_after();
-                    uint32_t d[kEpiGroup][2 * M];
+                // the unit's blocks in groups of kEpiGroup (group G in slot G mod
+                // kGroupSlots): one wait per group, the accumulators read kLd
+                // blocks at a time with one wait for the loads, every index
+                // static (the loops are unrolled with guards, so nothing moves
+                // to local memory)
+                constexpr int kLd = M <= 4 ? kEpiGroup : 2;
 #pragma unroll
-                    for (int j = 0; j < kEpiGroup; ++j)
-                        if (j < nb_g)
-                            tmem_ld<2 * M>(tbase + lane_base + kDCol0 + 32u * static_cast<uint32_t>(gs * kEpiGroup + j), d[j]);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&d_empty[gs]));
+                for (int gi = 0; gi < kSeg / kEpiGroup; ++gi) {
+                    const int b0 = gi * kEpiGroup;
+                    if (ok && b0 < U.bcount) {
+                        const int nb_g = min(kEpiGroup, U.bcount - b0);
+                        const int gs = Ge % kGroupSlots, gr = Ge / kGroupSlots;
+                        ok = __all_sync(0xffffffffu, tc_wait(smem_u32(&d_full[gs]), gr & 1, abort_flag, 32u, bad));
+                        if (ok) {
+                            tc_fence_after();
 #pragma unroll
-                    for (int j = 0; j < kEpiGroup; ++j) {
-                        if (j >= nb_g) break;
-                        const int bl = b0 + j;
-                        const uint32_t wsw = wsr[bl >> 1];
-                        const float ws = f16_bits_to_f32(static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
+                            for (int j0 = 0; j0 < kEpiGroup; j0 += kLd) {
+                                uint32_t d[kLd][2 * M];
 #pragma unroll
-                        for (int r = 0; r < M; ++r) {
-                            const float2 pr = pairs[bl * M + r];            // (activation scale, sum q)
-                            const float x = __fmaf_rn(16.0f, __uint_as_float(d[j][2 * r]), __uint_as_float(d[j][2 * r + 1]));
-                            const float dv = FMT == 0 ? __fsub_rn(x, pr.y) : __fmaf_rn(128.0f, x, -pr.y);
-                            acc[r] = __fadd_rn(acc[r], __fmul_rn(dv, __fmul_rn(ws, pr.x)));
-                            if (dots != nullptr && r < a.m && grow < md.n)
-                                dots[(static_cast<size_t>(r) * md.n + grow) * md.nb + U.seg * kSeg + bl] = __float2int_rn(dv);
+                                for (int j = 0; j < kLd; ++j)
+                                    if (j0 + j < nb_g)
+                                        tmem_ld<2 * M>(tbase + lane_base + kDCol0 +
+                                                           32u * static_cast<uint32_t>(gs * kEpiGroup + j0 + j),
+                                                       d[j]);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < kLd; ++j) {
+                                    if (j0 + j < nb_g) {
+                                        const int bl = b0 + j0 + j;          // static after unrolling
+                                        const uint32_t wsw = wsr[bl >> 1];
+                                        const float ws = f16_bits_to_f32(
+                                            static_cast<uint16_t>((bl & 1) ? (wsw >> 16) : (wsw & 0xffffu)));
+#pragma unroll
+                                        for (int r = 0; r < M; ++r) {
+                                            const float2 pr = pairs[bl * M + r];    // (activation scale, sum q)
+                                            const float x = __fmaf_rn(16.0f, __uint_as_float(d[j][2 * r]),
+                                                                      __uint_as_float(d[j][2 * r + 1]));
+                                            const float dv = FMT == 0 ? __fsub_rn(x, pr.y) : __fmaf_rn(128.0f, x, -pr.y);
+                                            acc[r] = __fadd_rn(acc[r], __fmul_rn(dv, __fmul_rn(ws, pr.x)));
+                                            if (dots != nullptr && r < a.m && grow < md.n)
+                                                dots[(static_cast<size_t>(r) * md.n + grow) * md.nb + U.seg * kSeg + bl] =
+                                                    __float2int_rn(dv);
+                                        }
+                                    }
+                                }
+                            }
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&d_empty[gs]));
                         }
+                        ++Ge;
                     }
                 }
                 if (!ok) break;
