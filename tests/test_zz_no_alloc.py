@@ -78,8 +78,12 @@ def test_static_scratch_call_allocates_nothing(tq):
 
 
 def test_static_scratch_refuses_sizes_beyond_its_limit(tq):
+    from _util import ws_offsets
     lib = tq.load()
-    assert lib.tq_ffn_static_workspace_bytes() >= lib.tq_ffn_workspace_bytes(8, 8192, 32768)
+    # the array holds the part of the FFN workspace the step it runs uses (the
+    # dp4a kernel's, which ends where the tensor-core sections begin) at the
+    # largest sizes it serves
+    assert lib.tq_ffn_static_workspace_bytes() == ws_offsets(8, 8192, 32768)["tc_hst"]
     # shapes only: nothing is read when the call refuses
     big = dict(hidden=8192 + 1024, inter=17408)
     g = tq._Weight(0x1000, 0x2000, big["inter"], big["hidden"], 0)
