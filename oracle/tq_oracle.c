@@ -82,11 +82,9 @@ float orc_f16_to_f32(uint16_t h) {
 /* The pages fix no byte layout ("its stored ternary blocks", PR #1154
  * Summary; "one packed weight format", bonsai-edge-serve README, kernels/).
  * Reading taken:
- *   2-bit: the field of weight k of row n in byte n*(k_dim/4) + k/4, bits
- *          2*(k%4)..2*(k%4)+1, least significant first, holds w + 1:
- *          field 0 -> -1, 1 -> 0, 2 -> +1 (3 is never written; read back
- *          as 0).  The packer's input codes keep their own convention:
- *          code 0 -> 0, 1 -> +1, 2 -> -1 (3 reads as 0).
+ *   2-bit: code of weight k of row n in byte n*(k_dim/4) + k/4, bits
+ *          2*(k%4)..2*(k%4)+1, least significant first; codes 0 -> 0,
+ *          1 -> +1, 2 -> -1 (3 is never written; read back as 0).
  *   1-bit: bit k%8 of byte n*(k_dim/8) + k/8; bit 1 -> +1, bit 0 -> -1.
  *   scales: one fp16 per 128-weight block per row, [n][k_dim/128]. */
 
@@ -96,10 +94,8 @@ void orc_pack2(const uint8_t *codes, int n, int k, uint8_t *packed) {
     for (int r = 0; r < n; r++)
         for (int j = 0; j < k / 4; j++) {
             uint8_t byte = 0;
-            for (int t = 0; t < 4; t++) {
-                const int w = orc_code2_value(codes[(size_t)r * k + 4 * j + t] & 3u);
-                byte |= (uint8_t)((unsigned)(w + 1) << (2 * t));
-            }
+            for (int t = 0; t < 4; t++)
+                byte |= (uint8_t)((codes[(size_t)r * k + 4 * j + t] & 3u) << (2 * t));
             packed[(size_t)r * (k / 4) + j] = byte;
         }
 }
@@ -108,8 +104,7 @@ void orc_unpack2(const uint8_t *packed, int n, int k, int8_t *w) {
     for (int r = 0; r < n; r++)
         for (int i = 0; i < k; i++) {
             uint8_t byte = packed[(size_t)r * (k / 4) + i / 4];
-            const int field = (byte >> (2 * (i % 4))) & 3;
-            w[(size_t)r * k + i] = (int8_t)(field == 3 ? 0 : field - 1);
+            w[(size_t)r * k + i] = orc_code2_value((byte >> (2 * (i % 4))) & 3u);
         }
 }
 
@@ -197,8 +192,7 @@ void orc_rotate_quant(const uint16_t *x, int m, int k, int8_t *q, float *s) {
 static int8_t weight_at(const uint8_t *packed, int fmt, int k, int n, int i) {
     if (fmt == 0) {
         uint8_t byte = packed[(size_t)n * (k / 4) + i / 4];
-        const int field = (byte >> (2 * (i % 4))) & 3;
-        return (int8_t)(field == 3 ? 0 : field - 1);
+        return orc_code2_value((byte >> (2 * (i % 4))) & 3u);
     }
     uint8_t byte = packed[(size_t)n * (k / 8) + i / 8];
     return ((byte >> (i % 8)) & 1u) ? 1 : -1;
