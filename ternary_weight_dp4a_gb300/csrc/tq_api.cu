@@ -174,6 +174,19 @@ tq_status check_fits_dp4a(const tq::Call &c) {
     return fits ? TQ_OK : TQ_ERR_UNSUPPORTED;
 }
 
+// A phase-B-only dp4a call shares tiles between CTAs (equal shares of the
+// units) through the workspace's segment sums and per-tile counts, when its
+// plan fits with them; otherwise it deals whole tiles.
+void share_tiles(tq::Call &c, float *gpart, unsigned *gcnt) {
+    c.gpart = gpart;
+    c.gcnt = gcnt;
+    cudaError_t e = cudaSuccess;
+    if (!tq::call_fits(c, &e)) {
+        c.gpart = nullptr;
+        c.gcnt = nullptr;
+    }
+}
+
 tq::Call dp4a_call(const tq_weight *gate, const tq_weight *up, const tq_weight *down, int fmt) {
     tq::Call c{};
     c.fmt = fmt;
@@ -403,6 +416,7 @@ tq_status tq_gemv(const tq_weight *w, const int8_t *q, const float *s, int32_t m
         return cuda_status(e);
     }
     tq::Call c = dp4a_call(nullptr, nullptr, w, w->fmt);
+    share_tiles(c, reinterpret_cast<float *>(wsb + L.part), reinterpret_cast<unsigned *>(wsb + L.cnt));
     if ((st = check_fits_dp4a(c)) != TQ_OK) return st;
     c.err = err;
     for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
@@ -565,6 +579,7 @@ tq_status tq_ffn_stage_down(const tq_weight *down, int32_t m, float *y, void *wo
         return cuda_status(e);
     }
     tq::Call c = dp4a_call(nullptr, nullptr, down, down->fmt);
+    share_tiles(c, P.part_b, P.cnt_b);
     if ((st = check_fits_dp4a(c)) != TQ_OK) return st;
     for (int r0 = 0; r0 < m && e == cudaSuccess; r0 += tq::kMaxRowsPerPass) {
         c.m = pass_rows(m, r0, tq::kMaxRowsPerPass);

@@ -42,7 +42,7 @@ cudaError_t dev_info(DevInfo *out) {
 }
 
 struct Plan {
-    uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt;
+    uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt, off_scr;
     size_t bytes;
     int slots, grid, tiles_max, nseg_max;
     Deal deal_a, deal_b;
@@ -51,6 +51,26 @@ struct Plan {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// A phase-B-only launch splits tiles between CTAs (equal shares of the
+// units) when the caller gave it the global segment sums and counts, their
+// scratch stays small, and it pays: the whole-tile deal's busiest CTA has
+// more than 1.15 x the average share, and a share spans at least two tiles
+// and 24 units, so that the cross-CTA fold of the shared tiles hides behind
+// other units (measured on GB300: a 5120 x 17408 GEMV, 2 or 3 tiles of 17
+// units per CTA, 17.3 -> 15.9 us at m = 1; GEMVs of 512 to 5120 rows with k
+// of 4096 or 5120, shares of 1 to 9 units, slower by 1.6 to 2.4 us).
+bool split_b(const Call &c, int sms) {
+    if (c.do_a || c.gcnt == nullptr || c.gpart == nullptr) return false;
+    const int uptB = ceil_div(c.wb.k / kBlock, kSegBlocks);
+    if (static_cast<size_t>(2) * uptB * c.m * kTileRows * 4 > 32768) return false;
+    const long long tiles = ceil_div(c.wb.n, kTileRows);
+    const long long G = std::min<long long>(sms, tiles);
+    const double share = static_cast<double>(tiles) / static_cast<double>(sms);     // tiles per CTA when split
+    const double busiest = static_cast<double>((tiles + G - 1) / G);
+    return share >= 2.0 && share * uptB >= 24.0 && busiest > 1.15 * share;
+}
+
 
 // q or q + 1 tiles per CTA.
 Deal uniform_deal(int ntiles, int G) {
@@ -94,7 +114,9 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     const int tilesA = ceil_div(nA, kTileRows), tilesB = ceil_div(nB, kTileRows);
     // a launch running both phases needs every CTA resident (phase B waits on
     // blocks of h other CTAs rotate): one CTA per SM
-    p->grid = (c.do_a && c.do_b) ? d.sms : std::max(1, std::min(d.sms, std::max(tilesA, tilesB)));
+    p->grid = (c.do_a && c.do_b) ? d.sms
+              : split_b(c, d.sms) ? std::max(1, std::min(d.sms, tilesB * ceil_div(kB / kBlock, kSegBlocks)))
+                           : std::max(1, std::min(d.sms, std::max(tilesA, tilesB)));
     const int G = p->grid;
     const int nbA = kA / kBlock, nbB = kB / kBlock;
     const int uptA = 2 * ceil_div(nbA, kSegBlocks), uptB = ceil_div(nbB, kSegBlocks);
@@ -103,6 +125,16 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     const int tpcA = c.do_a ? p->deal_a.lv[0] : 0, tpcB = c.do_b ? p->deal_b.lv[0] : 0;
     p->tiles_max = std::max(1, std::max(tpcA, tpcB));
     p->nseg_max = std::max(1, uptB);
+    // a phase-B-only launch with split tiles: an equal share of the units
+    // spans at most ceil(share / upt) + 1 tiles; two of them may be shared
+    // and folded from a scratch of all their segment sums
+    size_t scr = 0;
+    if (split_b(c, d.sms)) {
+        const long long U = static_cast<long long>(tilesB) * uptB;
+        const int share = static_cast<int>((U + G - 1) / G);
+        p->tiles_max = std::max(p->tiles_max, ceil_div(share, uptB) + 1);
+        scr = static_cast<size_t>(2) * uptB * c.m * kTileRows * 4;
+    }
     const size_t actA = static_cast<size_t>(nbA) * kBlock * c.m, snA = static_cast<size_t>(nbA) * c.m * 8;
     const size_t actB = static_cast<size_t>(nbB) * kBlock * c.m, snB = static_cast<size_t>(nbB) * c.m * 8;
     const size_t part = static_cast<size_t>(tpcA * uptA + tpcB * uptB) * c.m * kTileRows * 4;
@@ -111,7 +143,7 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     // and written 16 bytes at a time)
     constexpr size_t kAlign = 128;
     const size_t fixed = 1024 /* alignment slack */ + align_up(actA, kAlign) + align_up(snA, kAlign) + align_up(actB, kAlign) +
-                         align_up(snB, kAlign) + align_up(part, kAlign) + align_up(ints, kAlign);
+                         align_up(snB, kAlign) + align_up(part, kAlign) + align_up(ints, kAlign) + align_up(scr, kAlign);
     const size_t budget = static_cast<size_t>(d.smem_optin) - 2048;   // static shared memory < 1 KB
     if (fixed >= budget) return false;
     int slots = static_cast<int>(std::min<size_t>(kMaxSlots, (budget - fixed) / (kCodesSlot + kScalesSlot)));
@@ -133,6 +165,8 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     off = align_up(off + part, kAlign);
     p->off_tcnt = static_cast<uint32_t>(off);
     off = align_up(off + ints, kAlign);
+    p->off_scr = static_cast<uint32_t>(off);
+    off = align_up(off + scr, kAlign);
     p->bytes = off + 1024;
     return true;
 }
@@ -197,6 +231,11 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.off_snh = p.off_snh;
     a.off_part = p.off_part;
     a.off_tcnt = p.off_tcnt;
+    a.off_scr = p.off_scr;
+    if (split_b(c, d.sms)) {
+        a.gpart = c.gpart;
+        a.gcnt = c.gcnt;
+    }
     a.tiles_max = p.tiles_max;
     a.nseg_max = p.nseg_max;
     a.in_mode = c.in_mode;

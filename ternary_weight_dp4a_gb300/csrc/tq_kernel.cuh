@@ -105,6 +105,7 @@ struct KArgs {
     // (scale, magic - sum) pairs | phase B activation + pairs | segment sums |
     // int counters: units per tile, tiles folded, phase B segment state
     uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt;
+    uint32_t off_scr;         // phase-B-only launches with split tiles: two tiles' segment sums
     int tiles_max, nseg_max;
     // phase A input
     int in_mode;
@@ -139,6 +140,13 @@ struct KArgs {
     // one ticket per launch, so launch e's CTAs hold tickets [e G, (e + 1) G)
     unsigned *segready;
     unsigned long long *ticket;
+    // phase-B-only launches: when gcnt is set, CTA c takes an equal share
+    // [c U / G, (c + 1) U / G) of the U units in tile-major order, and a tile
+    // shared with a neighbouring CTA is folded by the CTA that completes it:
+    // gpart [tiles][segments][M][16] its segment sums, gcnt [tiles] units
+    // counted (zero between launches)
+    float *gpart;
+    unsigned *gcnt;
     unsigned *err;            // wait that ran out: bit 0 producer (slot free), 1 producer drain,
                               // 2 consumer (slot data), 3 consumer (slot issued), 4 producer
                               // (input staged), 6 phase B (segment of h); bit 5 is unused
@@ -611,7 +619,8 @@ __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, in
 
 // BO: a launch of phase B alone (a GEMV, or the down projection of a staged
 // h), compiled separately: no phase-A code, the whole input staged up front,
-// units tile-major.
+// units tile-major (whole tiles per CTA, or equal shares of the units with
+// the shared tiles folded across CTAs, see KArgs::gcnt).
 template <int FMT, int M, bool BO>
 __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -645,7 +654,17 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
 
     const PhaseGeo ga = (!BO && a.do_a) ? phase_geo(a.mat[0].n, a.mat[0].k, 2, G, cta, false, a.deal_a) : PhaseGeo{};
     const PhaseGeo gb = a.do_b ? phase_geo(a.mat[2].n, a.mat[2].k, 1, G, cta, true, a.deal_b) : PhaseGeo{};
-    const int total = ga.units + gb.units;
+    // a phase-B-only launch with split tiles: this CTA's units [u0, u1) of
+    // the tile-major order, from (global) tile t0 on
+    const bool split = BO && a.gcnt != nullptr;
+    int u0 = 0, u1 = gb.units;
+    if (split) {
+        const long long U = static_cast<long long>(gb.ntiles) * gb.upt;
+        u0 = static_cast<int>(cta * U / G);
+        u1 = static_cast<int>((cta + 1) * U / G);
+    }
+    const int t0 = split ? u0 / max(gb.upt, 1) : 0;
+    const int total = split ? u1 - u0 : ga.units + gb.units;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -678,7 +697,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
             // weights are read once per launch: evict them first, keeping
             // activations and other kernels' data in L2
             const uint64_t wpol = l2_policy_evict_first();
-            UnitPos u{0, in_a ? k : k - ga.units};
+            UnitPos u{0, in_a ? k : k - ga.units + (split ? u0 : 0)};
             unit_advance(u, 0, in_a ? max(ga.upt, 1) : bext);
             int slot = k % S, round = k / S;
             for (; k < total && ok; k += kProducerLanes) {
@@ -695,10 +714,10 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                     seg = u.inner - mi * P.nseg;
                 } else {
                     seg = BO ? u.inner : u.outer;
-                    lt = BO ? u.outer : u.inner;
+                    lt = BO ? u.outer - t0 : u.inner;
                     mi = 2;
                 }
-                const int tile = phase_tile(P, G, lt);
+                const int tile = split ? t0 + lt : phase_tile(P, G, lt);
                 const MatDesc &md = a.mat[mi];
                 if (k >= a.prologue_slots && k < a.prologue_slots + kProducerLanes &&
                     !(ok = mbar_wait(smem_u32(&input_bar), 0))) {
@@ -828,7 +847,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
         int kp = 0, slot = 0, round = 0;
         bool in_a = !BO && ga.units > 0;
         const int bext = max(BO ? gb.upt : gb.count, 1);   // phase B's inner extent
-        UnitPos u{0, 0};
+        UnitPos u{0, split ? u0 : 0};
         int staged_seg = -1;
         for (;;) {
             int k = 0;
@@ -856,7 +875,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                 seg = u.inner - mi * P.nseg;
             } else {
                 seg = BO ? u.inner : u.outer;
-                lt = BO ? u.outer : u.inner;
+                lt = BO ? u.outer - t0 : u.inner;
                 mi = 2;
                 if (!BO && seg != staged_seg) {
                     if (!stage_segment_b<FMT, M>(a, P, seg, act_h, sn_h, segst, s_epoch, lane)) {
@@ -885,7 +904,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                 bad |= 4u;
             }
             if (!ok) break;
-            const int tile = phase_tile(P, G, lt);
+            const int tile = split ? t0 + lt : phase_tile(P, G, lt);
             const MatDesc &md = a.mat[mi];
             const uint8_t *cs = codes_ring + static_cast<size_t>(slot) * kCodesSlot;
             const int bcount = min(kSegBlocks, P.nb - seg * kSegBlocks);
@@ -929,13 +948,43 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                 for (int mm = 0; mm < M; ++mm) pu[mm * kTileRows + (lane >> 1)] = acc[mm];
             }
             __syncwarp();
+            // this CTA's units of the tile: all of them, or (split tiles) the
+            // ones inside [u0, u1), local units i_lo .. i_lo + nloc - 1
+            const int tb = tile * P.upt;
+            const int nloc = split ? min(u1, tb + P.upt) - max(u0, tb) : P.upt;
             int last = 0;
             if (lane == 0) {
                 __threadfence_block();
-                last = atomicAdd(&(in_a ? tcnt_a : tcnt_b)[lt], 1) == P.upt - 1;
+                last = atomicAdd(&(in_a ? tcnt_a : tcnt_b)[lt], 1) == nloc - 1;
             }
             if (!__shfl_sync(0xffffffffu, last, 0)) continue;
             __threadfence_block();
+            // a tile shared with another CTA: publish this CTA's segment sums
+            // and count its units in; the CTA whose count completes the tile
+            // gathers all of them into its scratch and folds them there
+            float *tile_sums = nullptr;
+            if (split && nloc < P.upt) {
+                const int i_lo = max(u0, tb) - u0, s_lo = max(u0, tb) - tb;
+                const size_t w = static_cast<size_t>(M) * kTileRows;
+                float *gp = a.gpart + static_cast<size_t>(tb) * w;
+                for (int e = lane; e < nloc * static_cast<int>(w); e += 32)
+                    gp[s_lo * w + e] = part_b[static_cast<size_t>(i_lo) * w + e];
+                __syncwarp();
+                int done = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    done = atom_add_acq_rel_gpu(a.gcnt + tile, static_cast<unsigned>(nloc)) + nloc ==
+                           static_cast<unsigned>(P.upt);
+                }
+                if (!__shfl_sync(0xffffffffu, done, 0)) continue;
+                float *scr = reinterpret_cast<float *>(base + a.off_scr) + (lt == 0 ? 0 : static_cast<size_t>(P.upt) * w);
+                for (int e = lane; e < P.upt * static_cast<int>(w); e += 32) scr[e] = __ldcg(gp + e);
+                if (lane == 0) a.gcnt[tile] = 0u;
+                __syncwarp();
+                tile_sums = scr;
+            } else if (split) {
+                tile_sums = part_b + static_cast<size_t>(tb - u0) * M * kTileRows;
+            }
 
             // ---- the tile's last unit: fold its segment sums with the pairwise
             // tree and store h (phase A) or y (phase B).  A tile's units are
@@ -945,7 +994,8 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
             const int row = tile * kTileRows + rr16;
             const bool tmaj = in_a || BO;
             const size_t ustride = static_cast<size_t>(tmaj ? 1 : P.count) * M * kTileRows;
-            float *pt = (in_a ? part_a : part_b) + static_cast<size_t>(lt) * (tmaj ? P.upt : 1) * M * kTileRows +
+            float *pt = (tile_sums != nullptr ? tile_sums
+                                              : (in_a ? part_a : part_b) + static_cast<size_t>(lt) * (tmaj ? P.upt : 1) * M * kTileRows) +
                         r * kTileRows + rr16;
             for (int k2 = 0; 2 * k2 < M; ++k2) {
                 const int ra = r + 2 * k2;

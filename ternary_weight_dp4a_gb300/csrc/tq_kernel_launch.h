@@ -43,6 +43,11 @@ struct Call {
     const float *sb;
     float *y;
     int32_t *dots;
+    // phase-B-only launches: segment sums [tiles][segments][m][16] and unit
+    // counts [tiles] (zero between launches) of 16-row tiles shared between
+    // CTAs; null keeps whole tiles per CTA
+    float *gpart;
+    unsigned *gcnt;
     unsigned *segready;                 // per segment of h: rotated 128-blocks (A+B launches)
     unsigned long long *ticket;         // launch tickets (A+B launches)
     unsigned *err;

@@ -18,14 +18,18 @@
 //     [blocks][8] |
 //   part_a f32 [2][inter/128 tiles][hidden/1024 segments][8][128] |
 //   part_b f32 [hidden/128 tiles][inter/1024 segments][8][128] (segment sums) |
-//   cnt_a u32 [inter/128 tiles] | cnt_b u32 [hidden/128 tiles] (units counted
-//     per tile; zero between launches) | ybuf2 f32 [m][hidden] (the stack's
-//     second activation buffer: layers alternate between ybuf and ybuf2)
+//   cnt_a u32 [inter/128 tiles] | cnt_b u32 [hidden/16] (units counted per
+//     tile, 128-row tiles of the tensor-core kernel or 16-row tiles of the
+//     dp4a kernel's down projection alone, whose segment sums share part_b;
+//     zero between launches) | ybuf2 f32 [m][hidden] (the stack's second
+//     activation buffer: layers alternate between ybuf and ybuf2)
 //
 // GEMV workspace (m rows, n x k):
-//   err u32 | cnt u32 [n/128 tiles] | operand (2 KB per 128-block of k, whole
-//   segments) | pairs (f32 scale, f32 sum q) [blocks][8] |
-//   part f32 [n/128 tiles][k/1024 segments][8][128]
+//   err u32 | cnt u32 [n/16] (units counted per tile: 128-row tiles of the
+//   tensor-core kernel, 16-row tiles the dp4a kernel shares between CTAs) |
+//   operand (2 KB per 128-block of k, whole segments) | pairs (f32 scale, f32
+//   sum q) [blocks][8] | part f32 [n/128 tiles][k/1024 segments][8][128]
+//   (segment sums; the dp4a kernel's [n/16][k/1024][m <= 4][16] fit in it)
 #pragma once
 
 #include <cstddef>
@@ -72,7 +76,7 @@ constexpr FfnWorkspace ffn_layout(int64_t m, int64_t hidden, int64_t inter) {
     w.part_a = off; off = ws_round(off + 2 * tc_ws_partials(inter, hidden));
     w.part_b = off; off = ws_round(off + tc_ws_partials(hidden, inter));
     w.cnt_a = off; off = ws_round(off + static_cast<size_t>(ws_cdiv(inter, 128)) * 4);
-    w.cnt_b = off; off = ws_round(off + static_cast<size_t>(ws_cdiv(hidden, 128)) * 4);
+    w.cnt_b = off; off = ws_round(off + static_cast<size_t>(ws_cdiv(hidden, 16)) * 4);
     w.ybuf2 = off; off = ws_round(off + static_cast<size_t>(m * hidden) * 4);
     w.total = off;
     return w;
@@ -86,7 +90,7 @@ constexpr GemvWorkspace gemv_layout(int64_t n, int64_t k) {
     GemvWorkspace w{};
     size_t off = 0;
     w.err = off; off = ws_round(off + 4);
-    w.cnt = off; off = ws_round(off + static_cast<size_t>(ws_cdiv(n, 128)) * 4);
+    w.cnt = off; off = ws_round(off + static_cast<size_t>(ws_cdiv(n, 16)) * 4);
     w.operand = off; off = ws_round(off + tc_ws_operand(k));
     w.pairs = off; off = ws_round(off + tc_ws_pairs(k));
     w.part = off; off = ws_round(off + tc_ws_partials(n, k));

@@ -33,7 +33,7 @@ def ws_offsets(m, hidden, inter):
                          ("tc_hst", passes * seg_blocks * 2048), ("tc_hsn", passes * seg_blocks * 64),
                          ("part_a", 2 * cdiv(inter, B) * cdiv(hidden // B, 8) * 8 * B * 4),
                          ("part_b", cdiv(hidden, B) * cdiv(inter // B, 8) * 8 * B * 4),
-                         ("cnt_a", cdiv(inter, B) * 4), ("cnt_b", cdiv(hidden, B) * 4),
+                         ("cnt_a", cdiv(inter, B) * 4), ("cnt_b", cdiv(hidden, 16) * 4),
                          ("ybuf2", m * hidden * 4)):
         o[name] = off
         off = round_up(off + nbytes, 256)

@@ -70,14 +70,14 @@ def test_workspace_bytes(lib):
     dp4a = 5120 + 256 + 34816 + 17408 + 768 + 768 + 20480 + 256 + 256 + 17408 + 1280 + 69632
     # tensor-core part: operand copy of h, 136 blocks x 2 KB | its pairs 136 x 8 x 8 |
     # segment sums of gate and up, 2 x 136 tiles x 5 segments x 8 rows x 128 x 4 |
-    # of down, 40 tiles x 17 segments x 4096 | tile counts 136 x 4 -> 768, 40 x 4 -> 256 |
+    # of down, 40 tiles x 17 segments x 4096 | tile counts 136 x 4 -> 768, 320 x 4 -> 1280 |
     # second stack buffer 20480
-    tc = 136 * 2048 + 136 * 64 + 2 * 136 * 5 * 4096 + 40 * 17 * 4096 + 768 + 256 + 20480
+    tc = 136 * 2048 + 136 * 64 + 2 * 136 * 5 * 4096 + 40 * 17 * 4096 + 768 + 1280 + 20480
     assert lib.tq_ffn_workspace_bytes(1, 5120, 17408) == dp4a + tc
     assert lib.tq_ffn_workspace_bytes(0, 5120, 17408) == 0
-    # GEMV: err 256 | tile counts 136 x 4 -> 768 | operand 40 blocks x 2 KB |
+    # GEMV: err 256 | tile counts 1088 x 4 = 4352 | operand 40 blocks x 2 KB |
     # pairs 40 x 64 | segment sums 136 tiles x 5 segments x 4096
-    assert lib.tq_gemv_workspace_bytes(1, 17408, 5120) == 256 + 768 + 40 * 2048 + 40 * 64 + 136 * 5 * 4096
+    assert lib.tq_gemv_workspace_bytes(1, 17408, 5120) == 256 + 4352 + 40 * 2048 + 40 * 64 + 136 * 5 * 4096
     assert lib.tq_gemv_workspace_bytes(0, 17408, 5120) == 0
 
 

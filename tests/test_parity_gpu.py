@@ -75,9 +75,10 @@ def test_rotate_quant_bit_exact(tq, orc, m, k, outliers):
 # the tiny config, ragged and multi-tile shapes, the FFN's K, and the
 # full-attention projections of the model family the pages describe
 # (head_dim 256, 8:1 GQA with 2 KV heads: q 4096 x 5120, k/v 512 x 5120,
-# o 5120 x 4096)
+# o 5120 x 4096), and the FFN's down projection alone (5120 x 17408: the
+# dp4a kernel shares its 320 tiles between CTAs in equal shares of units)
 GEMV_SHAPES = [(512, 256), (1000, 384), (77, 1152), (4101, 5120), (96, 17408),
-               (4096, 5120), (512, 5120), (5120, 4096)]
+               (4096, 5120), (512, 5120), (5120, 4096), (5120, 17408)]
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
