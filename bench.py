@@ -521,7 +521,7 @@ def run_ours(args, rank, world, local):
     return result
 
 
-def profile_steps(n: int, engine: str = "tcgen05", m: int = 1):
+def profile_steps(n: int, engine: str = "dp4a", m: int = 1):
     """n eager m-row steps over the weight sets (no timing, no JSON line)."""
     import torch
     from ternary_weight_dp4a_gb300 import build as tqbuild
@@ -539,7 +539,7 @@ def profile_steps(n: int, engine: str = "tcgen05", m: int = 1):
     torch.cuda.synchronize()
 
 
-def profile_gemv(n: int, engine: str = "tcgen05"):
+def profile_gemv(n: int, engine: str = "dp4a"):
     """n eager m = 1 tq_gemv calls on the 17408 x 5120 gate shape, rotating
     over the weight sets' gate matrices (no timing, no JSON line)."""
     import torch
@@ -664,6 +664,25 @@ def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1, extras: bool 
     return out
 
 
+def probe_mma_rate():
+    """Build csrc/probes/tq_mma_rate.cu for sm_103a into a temporary
+    directory and run it: time per tcgen05.mma (kind::f8f6f4, M = 128,
+    K = 32) at N = 16..256 with A in tensor or shared memory."""
+    import shutil
+    import subprocess
+    import tempfile
+    src = os.path.join(ROOT, "ternary_weight_dp4a_gb300", "csrc", "probes", "tq_mma_rate.cu")
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    with tempfile.TemporaryDirectory() as d:
+        exe = os.path.join(d, "tq_mma_rate")
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src], check=True)
+        r = subprocess.run([exe], capture_output=True, text=True)
+        print(r.stdout, end="")
+        if r.returncode != 0:
+            print(r.stderr, end="")
+            raise SystemExit(r.returncode)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -679,10 +698,15 @@ def main():
                          "(a small, untimed case for a profiler to capture)")
     ap.add_argument("--profile-gemv", type=int, default=0,
                     help="run this many eager m = 1 GEMVs on the 17408 x 5120 gate shape and exit")
-    ap.add_argument("--profile-engine", choices=list(ENGINES), default="tcgen05",
-                    help="kernel for --profile-steps / --profile-gemv")
+    ap.add_argument("--profile-engine", choices=list(ENGINES), default="dp4a",
+                    help="kernel for --profile-steps / --profile-gemv (default: the default engine's)")
     ap.add_argument("--profile-rows", type=int, default=1, help="rows per step for --profile-steps")
+    ap.add_argument("--probe-mma-rate", action="store_true",
+                    help="build and run the tcgen05.mma throughput probe (csrc/probes/tq_mma_rate.cu) and exit")
     args = ap.parse_args()
+    if args.probe_mma_rate:
+        probe_mma_rate()
+        return
     if args.warmup < 3:
         args.warmup = 3
 
