@@ -44,7 +44,7 @@ cudaError_t dev_info(DevInfo *out) {
 struct Plan {
     uint32_t off_scales, off_act, off_sn, off_acth, off_snh, off_part, off_tcnt, off_scr;
     size_t bytes;
-    int slots, grid, tiles_max, nseg_max;
+    int slots, lanes, grid, tiles_max, nseg_max;
     Deal deal_a, deal_b;
 };
 
@@ -147,9 +147,12 @@ bool make_plan(const Call &c, const DevInfo &d, Plan *p) {
     const size_t budget = static_cast<size_t>(d.smem_optin) - 2048;   // static shared memory < 1 KB
     if (fixed >= budget) return false;
     int slots = static_cast<int>(std::min<size_t>(kMaxSlots, (budget - fixed) / (kCodesSlot + kScalesSlot)));
-    slots -= slots % kProducerLanes;      // each slot filled by one producer lane
-    if (slots < 2 * kProducerLanes) return false;
+    // one or two rows: 6 producer lanes where 12 slots or more fit
+    const int lanes = c.m <= 2 && slots - slots % kProducerLanesMax >= 2 * kProducerLanesMax ? kProducerLanesMax : 4;
+    slots -= slots % lanes;               // each slot filled by one producer lane
+    if (slots < 2 * lanes) return false;
     p->slots = slots;
+    p->lanes = lanes;
     size_t off = static_cast<size_t>(slots) * kCodesSlot;
     p->off_scales = static_cast<uint32_t>(off);
     off += static_cast<size_t>(slots) * kScalesSlot;
@@ -223,6 +226,7 @@ cudaError_t launch_call(const Call &c, cudaStream_t stream) {
     a.deal_a = p.deal_a;
     a.deal_b = p.deal_b;
     a.slots = p.slots;
+    a.lanes = p.lanes;
     a.prologue_slots = std::min(p.slots, kPrologueSlots);
     a.off_scales = p.off_scales;
     a.off_act = p.off_act;

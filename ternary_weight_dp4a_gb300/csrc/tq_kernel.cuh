@@ -50,12 +50,16 @@ constexpr int kMaxRowsPerPass = 4;
 // fully unrolled; fewer: a smaller hot loop)
 constexpr int kOneRowBlocksPerIter = 8;
 constexpr int kRowsBlocksPerIter = 4;
-// Producer lanes; lane l issues units k = l (mod kProducerLanes).  The ring
-// has a multiple of kProducerLanes slots, so every fill of a slot comes from
-// one lane, in order: when that lane waits for a slot's previous fill to be
+// Producer lanes; lane l issues units k = l (mod L), L = KArgs::lanes.  The
+// ring has a multiple of L slots, so every fill of a slot comes from one
+// lane, in order: when that lane waits for a slot's previous fill to be
 // released, every earlier release of the slot has happened, and the phase
-// parity it waits on cannot alias an older phase.
-constexpr int kProducerLanes = 4;
+// parity it waits on cannot alias an older phase.  One or two rows consume a
+// unit fastest and want more copies in the issue pipe (6 lanes where the
+// ring has 12 slots or more); from four rows on, 4 lanes leave the compute
+// warps more issue slots.
+constexpr int kProducerLanesMax = 6;
+static_assert(kMaxSlots % kProducerLanesMax == 0 && kMaxSlots % 4 == 0, "a full ring splits evenly among the lanes");
 constexpr int kTilesPerHBlock = kBlock / kTileRows;   // 16-row tiles per 128-block of h
 
 // How a phase's 16-row tiles are dealt to the CTAs.  CTA d (in dealing
@@ -99,7 +103,8 @@ struct KArgs {
     MatDesc mat[3];           // phase A: gate, up; phase B: mat[2]
     int do_a, do_b;
     Deal deal_a, deal_b;      // tiles per CTA of each phase
-    int slots;                // ring slots
+    int slots;                // ring slots (a multiple of lanes)
+    int lanes;                // producer lanes issuing the units
     int prologue_slots;       // units the producer issues before the input is staged
     // dynamic shared memory: ring codes | ring scales | phase A activation +
     // (scale, magic - sum) pairs | phase B activation + pairs | segment sums |
@@ -682,13 +687,14 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        // Lanes 0..kProducerLanes-1 each issue every kProducerLanes-th unit,
+        // Lanes 0..L-1 each issue every L-th unit (L = a.lanes),
         // so several units are in the issue pipe at once; unit positions and
         // (slot, round) = divmod(k, S) advance incrementally.  Only the first
         // prologue_slots units go out before the consumers have staged the
         // input: the input's loads would otherwise queue behind a full ring
         // of weight copies.
-        if (lane < kProducerLanes) {
+        const int L = a.lanes;
+        if (lane < L) {
             bool ok = true;
             unsigned bad = 0u;
             int k = lane;
@@ -700,7 +706,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
             UnitPos u{0, in_a ? k : k - ga.units + (split ? u0 : 0)};
             unit_advance(u, 0, in_a ? max(ga.upt, 1) : bext);
             int slot = k % S, round = k / S;
-            for (; k < total && ok; k += kProducerLanes) {
+            for (; k < total && ok; k += L) {
                 if (in_a && k >= ga.units) {
                     in_a = false;
                     u = UnitPos{0, k - ga.units};
@@ -719,7 +725,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                 }
                 const int tile = split ? t0 + lt : phase_tile(P, G, lt);
                 const MatDesc &md = a.mat[mi];
-                if (k >= a.prologue_slots && k < a.prologue_slots + kProducerLanes &&
+                if (k >= a.prologue_slots && k < a.prologue_slots + L &&
                     !(ok = mbar_wait(smem_u32(&input_bar), 0))) {
                     bad |= 16u;
                     break;
@@ -745,8 +751,8 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                 if (sct)
                     tma_load_2d(smem_u32(scales_ring + static_cast<size_t>(slot) * (kScalesSlot / 2)), &md.tm_scales,
                                 seg * kSegBlocks, tile * kTileRows, fb, wpol);
-                unit_advance(u, kProducerLanes, in_a ? P.upt : bext);
-                slot += kProducerLanes;
+                unit_advance(u, L, in_a ? P.upt : bext);
+                slot += L;
                 if (slot >= S) {
                     slot -= S;
                     ++round;
@@ -754,11 +760,11 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
             }
             // no copy may still be landing in shared memory when the CTA
             // exits.  Every fill of a slot comes from one lane, so this lane's
-            // last S / kProducerLanes units are the last fills of its slots
+            // last S / L units are the last fills of its slots
             // (earlier fills were consumed before their slot was refilled):
             // wait for those, newest first.  When the consumers took every
             // unit, all have landed and each check returns at once.
-            for (int kk = k - kProducerLanes, n = 0; kk >= 0 && n < S / kProducerLanes; kk -= kProducerLanes, ++n)
+            for (int kk = k - L, n = 0; kk >= 0 && n < S / L; kk -= L, ++n)
                 if (!mbar_wait(smem_u32(&full_bar[kk % S]), (kk / S) & 1)) {
                     bad |= 2u;
                     break;

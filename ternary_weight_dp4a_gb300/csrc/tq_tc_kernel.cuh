@@ -203,16 +203,20 @@ __device__ __forceinline__ void hilo_words(const int (&q)[4], uint32_t &whi, uin
 // ---------------------------------------------------------------------------
 // Bounded waits.  A wait gives up after ~0.5 s of clock cycles (or at once
 // when another role of the CTA has given up): it records its error bit in
-// *bad and raises the CTA's abort flag.
+// *bad and raises the CTA's abort flag.  Waits that only follow other waits
+// (the counter's and the fold warps' waits for finished work) get twice the
+// budget, so the wait that names the cause runs out first.
 // ---------------------------------------------------------------------------
+constexpr long long kFollowerBudgetCycles = 2 * kWaitBudgetCycles;
+
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned bit,
-                                        unsigned &bad) {
+                                        unsigned &bad, long long budget = kWaitBudgetCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) {
+        if (clock64() - t0 > budget) {
             bad |= bit;
             *abort_flag = 1;
             return false;
@@ -671,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             pdl_wait();
             int nj = 0;
             for (int k = 0; k < nunits; ++k) {
-                if (!tc_wait(smem_u32(&unit_done[k]), 0, abort_flag, 128u, bad)) break;
+                if (!tc_wait(smem_u32(&unit_done[k]), 0, abort_flag, 128u, bad, kFollowerBudgetCycles)) break;
                 const Unit U = unit_of(a, cta + k * G);
                 const TcMat &md = a.mat[U.mi];
                 unsigned *cnt = U.phase == 0 ? a.cnt_a + U.tile : a.cnt_b + U.tile;
@@ -866,7 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             job = j;
                             break;
                         }
-                        if (clock64() - t0 > kWaitBudgetCycles) {
+                        if (*abort_flag) break;
+                        if (clock64() - t0 > kFollowerBudgetCycles) {
                             bad |= 128u;
                             break;
                         }
