@@ -104,6 +104,7 @@ struct KArgs {
     int do_a, do_b;
     Deal deal_a, deal_b;      // tiles per CTA of each phase
     int slots;                // ring slots (a multiple of lanes)
+    int lazy_b;               // phase-B-only: stage the input by segments on demand
     int lanes;                // producer lanes issuing the units
     int prologue_slots;       // units the producer issues before the input is staged
     // dynamic shared memory: ring codes | ring scales | phase A activation +
@@ -163,8 +164,8 @@ struct KArgs {
 // order: phase A tile-major (tile, matrix, segment); phase B of a launch that
 // also runs phase A segment-major (segment, tile), so that a CTA needs the
 // segments of h in the order they become ready; a phase-B-only launch
-// (whole input staged up front) tile-major (tile, segment), so that a CTA
-// reads each tile's rows in one pass.
+// (its whole input present at the start) tile-major (tile, segment), so
+// that a CTA reads each tile's rows in one pass.
 struct PhaseGeo {
     int n, k, nb, nseg, upt, ntiles, dc, count, units;
     Deal deal;
@@ -457,13 +458,14 @@ __device__ __forceinline__ void unit_dp4a(const uint8_t *cs, bool codes3d, const
 
 // Stage blocks [b_begin, b_end) of int8 rows q [M][k] (+ fp32 s [M][k/128])
 // from global memory, warps w, w + nw, ... taking (row, block) pairs; each
-// warp loads a group of up to 4 blocks before working on any of them.
+// warp loads a group of up to 8 blocks (a segment of one row) before working
+// on any of them.
 template <int FMT, int M>
 __device__ __forceinline__ void stage_plain_range(const int8_t *__restrict__ q, const float *__restrict__ s, int k,
                                                   int b_begin, int b_end, uint8_t *act, float2 *sn, int w, int nw,
                                                   int lane) {
     const int nb = k / kBlock, cnt = b_end - b_begin;
-    constexpr int kGroup = 4;
+    constexpr int kGroup = 8;
     for (int p0 = w; p0 < M * cnt; p0 += kGroup * nw) {
         uint32_t wd[kGroup];
         float sc[kGroup];
@@ -623,8 +625,8 @@ __device__ __forceinline__ void rotate_h_block(const KArgs &a, int n, int hb, in
 }
 
 // BO: a launch of phase B alone (a GEMV, or the down projection of a staged
-// h), compiled separately: no phase-A code, the whole input staged up front,
-// units tile-major (whole tiles per CTA, or equal shares of the units with
+// h), compiled separately: no phase-A code, the input staged up front (or by
+// segments as warps first need them, KArgs::lazy_b), units tile-major (whole tiles per CTA, or equal shares of the units with
 // the shared tiles folded across CTAs, see KArgs::gcnt).
 template <int FMT, int M, bool BO>
 __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __grid_constant__ KArgs a) {
@@ -826,9 +828,12 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
         }
         if (ticketed && tid == 0) s_epoch = static_cast<unsigned>(ticket / static_cast<unsigned long long>(G));
         named_barrier(1, kConsumers);
-    } else if (BO) {
+    } else if (BO && !a.lazy_b) {
         // ---- a phase-B-only launch: its whole input is in memory already
-        // (the grid-dependency wait above); stage it once, all warps
+        // (the grid-dependency wait above); stage it once, all warps.  With
+        // lazy_b the first warp to need a segment stages it instead, as
+        // phase B does in a fused launch (a long input at one or two rows:
+        // no warp waits for the whole input before its first unit)
         if (a.bst != nullptr) {
             const uint4 *src = reinterpret_cast<const uint4 *>(a.bst);
             uint4 *dst = reinterpret_cast<uint4 *>(act_h);
@@ -883,7 +888,7 @@ __global__ void __launch_bounds__(kBoundThreads<FMT, M>, 1) tq_kernel(const __gr
                 seg = BO ? u.inner : u.outer;
                 lt = BO ? u.outer - t0 : u.inner;
                 mi = 2;
-                if (!BO && seg != staged_seg) {
+                if ((!BO || a.lazy_b) && seg != staged_seg) {
                     if (!stage_segment_b<FMT, M>(a, P, seg, act_h, sn_h, segst, s_epoch, lane)) {
                         ok = false;
                         bad |= 64u;
