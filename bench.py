@@ -521,7 +521,7 @@ def run_ours(args, rank, world, local):
     return result
 
 
-def profile_steps(n: int, engine: str = "dp4a", m: int = 1):
+def profile_steps(n: int, engine: str = "dp4a", m: int = 1, fmt: str = "2bit"):
     """n eager m-row steps over the weight sets (no timing, no JSON line)."""
     import torch
     from ternary_weight_dp4a_gb300 import build as tqbuild
@@ -529,7 +529,7 @@ def profile_steps(n: int, engine: str = "dp4a", m: int = 1):
     tqbuild.build()
     tq.load()
     set_engine(engine)
-    layers = make_weights(tq.FMT_TERNARY2, N_SETS, HIDDEN, INTER)
+    layers = make_weights(tq.FMT_TERNARY2 if fmt == "2bit" else tq.FMT_BINARY1, N_SETS, HIDDEN, INTER)
     x = synth.activation(m, HIDDEN, synth.SEED_ACT_BASE, 0.01, device="cuda")
     y = torch.empty((m, HIDDEN), dtype=torch.float32, device="cuda")
     ws = tq.ffn_workspace(m, HIDDEN, INTER)
@@ -664,17 +664,19 @@ def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1, extras: bool 
     return out
 
 
-def probe_mma_rate():
-    """Build csrc/probes/tq_mma_rate.cu for sm_103a into a temporary
-    directory and run it: time per tcgen05.mma (kind::f8f6f4, M = 128,
-    K = 32) at N = 16..256 with A in tensor or shared memory."""
+def run_probe(name: str):
+    """Build csrc/probes/<name>.cu for sm_103a into a temporary directory and
+    run it.  tq_mma_rate: time per tcgen05.mma (kind::f8f6f4, M = 128,
+    K = 32) at N = 16..256 with A in tensor or shared memory.  tq_lut_rate:
+    weights per cycle per SM of the 1-bit dp4a inner loop against 16- and
+    256-entry lookup tables."""
     import shutil
     import subprocess
     import tempfile
-    src = os.path.join(ROOT, "ternary_weight_dp4a_gb300", "csrc", "probes", "tq_mma_rate.cu")
+    src = os.path.join(ROOT, "ternary_weight_dp4a_gb300", "csrc", "probes", name + ".cu")
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     with tempfile.TemporaryDirectory() as d:
-        exe = os.path.join(d, "tq_mma_rate")
+        exe = os.path.join(d, name)
         subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src], check=True)
         r = subprocess.run([exe], capture_output=True, text=True)
         print(r.stdout, end="")
@@ -701,11 +703,18 @@ def main():
     ap.add_argument("--profile-engine", choices=list(ENGINES), default="dp4a",
                     help="kernel for --profile-steps / --profile-gemv (default: the default engine's)")
     ap.add_argument("--profile-rows", type=int, default=1, help="rows per step for --profile-steps")
+    ap.add_argument("--profile-fmt", choices=["2bit", "1bit"], default="2bit",
+                    help="weight format for --profile-steps")
     ap.add_argument("--probe-mma-rate", action="store_true",
                     help="build and run the tcgen05.mma throughput probe (csrc/probes/tq_mma_rate.cu) and exit")
+    ap.add_argument("--probe-lut-rate", action="store_true",
+                    help="build and run the 1-bit dp4a vs lookup-table probe (csrc/probes/tq_lut_rate.cu) and exit")
     args = ap.parse_args()
     if args.probe_mma_rate:
-        probe_mma_rate()
+        run_probe("tq_mma_rate")
+        return
+    if args.probe_lut_rate:
+        run_probe("tq_lut_rate")
         return
     if args.warmup < 3:
         args.warmup = 3
@@ -732,7 +741,7 @@ def main():
 
     rank, world, local = dist_setup()
     if args.profile_steps > 0:
-        profile_steps(args.profile_steps, args.profile_engine, args.profile_rows)
+        profile_steps(args.profile_steps, args.profile_engine, args.profile_rows, args.profile_fmt)
         return
     if args.profile_gemv > 0:
         profile_gemv(args.profile_gemv, args.profile_engine)
