@@ -273,6 +273,10 @@ def time_steps(step_fns, steps: int, warmup: int, world: int, sampler_gpu=None):
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # a ~100 us device sleep ahead of the start event: the host enqueues the
+    # event and the replays meanwhile, so the timed region holds the steps
+    # back to back and not the latency of the first launch after the sync
+    torch.cuda._sleep(200000)
     start.record()
     run(steps)
     end.record()
@@ -664,6 +668,55 @@ def cpu_oracle_baseline(budget_s: float, fmt: int = 0, m: int = 1, extras: bool 
     return out
 
 
+def reference_arm(steps: int, warmup: int, budget_s: float = 120.0):
+    """The oracle as it stands, on the host cores: exactly ``warmup`` untimed
+    and ``steps`` timed steps of the headline workload.  A step is the full FFN
+    layer step when ``steps`` of them fit in about ``budget_s`` seconds, else
+    the same fraction of every matrix's rows (rotate x, gate and up rows, SiLU
+    times up, down rows on the h of one full step taken first), so that any
+    --steps ends within a few minutes.  GB/s = weight bytes the timed steps
+    read / their time."""
+    from oracle import oracle
+    from ternary_weight_dp4a_gb300 import synth
+    oracle.build()
+    mats = _ffn_mats_host(0)
+    x = synth.activation(1, HIDDEN, synth.SEED_ACT_BASE, 0.01)
+    t0 = time.perf_counter()
+    full = oracle.ffn_step(*mats, 0, HIDDEN, INTER, x)
+    t_full = time.perf_counter() - t0
+    frac = min(1.0, budget_s / max(steps, 1) / t_full)
+    if frac >= 1.0:
+        def step():
+            oracle.ffn_step(*mats, 0, HIDDEN, INTER, x)
+        step_bytes = layer_bytes(HIDDEN, INTER, 0)
+        sample = "full FFN layer steps"
+    else:
+        rg, rd = max(1, int(INTER * frac)), max(1, int(HIDDEN * frac))
+        gate, gate_s, up, up_s, down, down_s = mats
+        g_p, g_s, u_p, u_s = gate[:rg], gate_s[:rg], up[:rg], up_s[:rg]
+        d_p, d_s = down[:rd], down_s[:rd]
+
+        def step():
+            q, s = oracle.rotate_quant(x)
+            g = oracle.gemv(g_p, g_s, 0, rg, HIDDEN, q, s)
+            u = oracle.gemv(u_p, u_s, 0, rg, HIDDEN, q, s)
+            oracle.silu_mul_bf16(g, u)
+            oracle.gemv(d_p, d_s, 0, rd, INTER, full["qh"], full["sh"])
+        step_bytes = 2 * rg * (HIDDEN // 4 + 2 * HIDDEN // 128) + rd * (INTER // 4 + 2 * INTER // 128)
+        sample = (f"{rg} of {INTER} gate/up rows and {rd} of {HIDDEN} down rows per step "
+                  f"(the same fraction {frac:.4f} of every matrix)")
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    sec = (time.perf_counter() - t0) / max(steps, 1)
+    return {"value": round(step_bytes / sec / 1e9, 4), "unit": "GB/s", "cores": oracle.get_threads(),
+            "kind": "oracle", "sample": f"{steps} timed steps after {warmup} untimed: {sample}, m=1, "
+                                        f"hidden {HIDDEN}, intermediate {INTER}, 2-bit",
+            "us_per_step": round(sec * 1e6, 1), "bytes_per_step": step_bytes}
+
+
 def run_probe(name: str):
     """Build csrc/probes/<name>.cu for sm_103a into a temporary directory and
     run it.  tq_mma_rate: time per tcgen05.mma (kind::f8f6f4, M = 128,
@@ -725,10 +778,9 @@ def main():
         # the reference arm is the CPU oracle, timed on rank 0's host cores only
         if rank != 0:
             return
-        base = cpu_oracle_baseline(args.cpu_budget)
-        steps = max(1, args.steps if args.steps < 4 else 1)
+        base = reference_arm(args.steps, args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s",
-                "n_gpus": world, "steps": steps, "warmup": 0,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(base["us_per_step"] / 1e3, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "int8xternary2->f32",
                 "data": "synthetic (seeded)",
