@@ -36,11 +36,12 @@ namespace tq {
 constexpr int kConsumerWarps = 15;      // compute warps (warp 15 is the producer)
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-// Thread count the compiler budgets registers for (the launch uses
-// kThreads): 544 caps 2-bit m = 3, 4 at 96 registers per thread, which
-// measured faster for them than 128 despite a few spills; the rest keep 128.
+// Thread count the compiler budgets registers for: the launch's own, so
+// every instantiation may use 128 registers per thread (2-bit m = 3, 4 once
+// measured faster capped at 96; with the hint-free barrier waits 128 is
+// faster: m = 4 step 47.6 -> 47.0 us, m = 8 95.2 -> 93.7 us).
 template <int FMT, int M>
-constexpr int kBoundThreads = (FMT == 0 && M >= 3) ? kThreads + 32 : kThreads;
+constexpr int kBoundThreads = kThreads;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kCodesSlot = 4096;        // 16 rows x 8 blocks of codes (2-bit: two 2 KB planes)
 constexpr int kScalesSlot = 256;        // 16 rows x 8 fp16 scales
