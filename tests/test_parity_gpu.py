@@ -81,9 +81,11 @@ GEMV_SHAPES = [(512, 256), (1000, 384), (77, 1152), (4101, 5120), (96, 17408),
                (4096, 5120), (512, 5120), (5120, 4096), (5120, 17408)]
 
 
+# m = 1, 2 over an input of 64 blocks or more (k = 17408) stage it by segments
+# on demand; the other cases stage it up front
 @pytest.mark.parametrize("fmt", [0, 1])
 @pytest.mark.parametrize("n,k", GEMV_SHAPES)
-@pytest.mark.parametrize("m", [1, 3, 8])
+@pytest.mark.parametrize("m", [1, 2, 3, 8])
 def test_gemv_bit_exact(tq, orc, fmt, n, k, m):
     import torch
     w = Mat(n, k, fmt, seed=synth.SEED_TINY_WEIGHT)
@@ -316,6 +318,28 @@ def test_ffn_workspace_counters_return_to_zero_and_stages_match_step(tq, orc):
         tq.ffn_stage_down(d.dev, m, y2, ws2)
     torch.cuda.synchronize()
     assert np.array_equal(y2.cpu().numpy().view(np.uint32), y_step.view(np.uint32))
+
+
+@pytest.mark.parametrize("m", [1, 2])
+def test_ffn_stages_long_intermediate_match_step(tq, orc, m):
+    """The down stage over a long staged h (intermediate 8192: 64 blocks,
+    staged by segments on demand at one or two rows) computes exactly the
+    one-launch step, and the step matches the oracle."""
+    import torch
+    hidden, inter = 1024, 8192
+    mats = ffn_mats(hidden, inter, 0)
+    x = _acts(m, hidden, 0.01)
+    y_step, _ = _ffn_gpu(tq, mats, x)
+    g, u, d = mats
+    ws2 = tq.ffn_workspace(m, hidden, inter)
+    y2 = torch.empty((m, hidden), dtype=torch.float32, device="cuda")
+    tq.ffn_stage_input(bf16_tensor(x), inter, ws2)
+    tq.ffn_stage_gateup(g.dev, u.dev, m, ws2)
+    tq.ffn_stage_down(d.dev, m, y2, ws2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y2.cpu().numpy().view(np.uint32), y_step.view(np.uint32))
+    ref = _ffn_orc(orc, mats, x)
+    assert np.array_equal(y_step.view(np.uint32), ref["y"].view(np.uint32))
 
 
 def test_ffn_gateup_standalone_matches_oracle(tq, orc):
