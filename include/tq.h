@@ -30,8 +30,10 @@
  *     identical bits: a dp4a kernel and a tensor-core kernel (weights decoded
  *     to e4m3 in tensor memory, tcgen05.mma against the int8 activation split
  *     into two exact e4m3 parts).  tq_set_engine chooses; the default uses the
- *     dp4a kernel, measured the faster on GB300 at every row count, wherever
- *     its shared-memory plan fits, and the tensor-core kernel elsewhere.
+ *     dp4a kernel, measured the faster on GB300 for the FFN step at every row
+ *     count and for the GEMV on every measured shape except a long input
+ *     (5120 x 17408) at 8 rows, wherever its shared-memory plan fits, and the
+ *     tensor-core kernel elsewhere.
  *   - Floating point is IEEE binary32 with the rounding of each step
  *     documented at the entry point; results do not depend on m, on the
  *     stream or on how many SMs the GPU has.
