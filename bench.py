@@ -430,7 +430,8 @@ def run_ours(args, rank, world, local):
             y_host.copy_(ys[1], non_blocking=True)
         return [lambda g=g, u=u, d=d: one(g, u, d) for g, u, d in layers]
 
-    e2e_steps = max(N_SETS, min(args.steps, 4000))
+    # at least 2000 steps (as the steady figure), whatever --steps is
+    e2e_steps = max(2000, min(args.steps, 4000))
     t_e2e, _ = time_steps(e2e_fns(), e2e_steps, N_SETS, world)
     e2e_ms = max_over_ranks(t_e2e, world) / e2e_steps
     e2e_value = world * lb / (e2e_ms * 1e-3) / 1e9
@@ -439,7 +440,7 @@ def run_ours(args, rank, world, local):
     for f in fns:
         f()
     torch.cuda.synchronize()
-    eager_steps = N_SETS * max(1, min(args.steps, 1000) // N_SETS)
+    eager_steps = N_SETS * (1000 // N_SETS)        # 1000 eager calls, whatever --steps is
     t0 = time.perf_counter()
     for i in range(eager_steps):
         fns[i % N_SETS]()
