@@ -63,3 +63,19 @@ def test_source_hash_leaves_out_host_only_sources(monkeypatch, tmp_path):
     assert bench.source_hash() == h0                 # host-only file: same hash
     (csrc / "k.cu").write_text("kernel, changed")
     assert bench.source_hash() != h0                 # kernel file: new hash
+
+
+def test_reference_arm_runs_the_requested_steps(monkeypatch):
+    """The reference arm times exactly --warmup untimed and --steps timed
+    oracle steps: whole layer steps when they fit the budget, else the same
+    fraction of every matrix's rows (bytes counted from the rows read)."""
+    monkeypatch.setattr(bench, "HIDDEN", 256)
+    monkeypatch.setattr(bench, "INTER", 512)
+    full = bench.reference_arm(2, 1, budget_s=30.0)
+    assert full["sample"].startswith("2 timed steps after 1 untimed: full FFN layer steps")
+    assert full["bytes_per_step"] == bench.layer_bytes(256, 512, 0)
+    assert full["kind"] == "oracle" and full["value"] > 0 and full["cores"] >= 1
+    part = bench.reference_arm(50, 3, budget_s=1e-6)
+    assert part["sample"].startswith("50 timed steps after 3 untimed: 1 of 512 gate/up rows and 1 of 256 down rows")
+    assert part["bytes_per_step"] == 2 * (256 // 4 + 2 * 256 // 128) + (512 // 4 + 2 * 512 // 128)
+    assert part["value"] > 0
